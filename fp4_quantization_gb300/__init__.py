@@ -1,0 +1,171 @@
+"""GB300 (sm_103a) block-scaled quantization: bf16 -> MXFP8 / NVFP4.
+
+Thin Python binding over libmxq.so, whose C ABI is declared in
+``include/mxq.h``.  The functions here carry the same names as the C entry
+points and only marshal arguments: they allocate outputs with torch when the
+caller does not pass them, pass raw device pointers and the current CUDA
+stream, and raise ``MxqError`` on a non-zero status.  Every step of the
+quantization runs in the library's kernels; there is no fallback path, and
+importing this package fails if libmxq.so cannot be loaded.
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+
+ROWWISE = 1
+COLWISE = 2
+DBIAS = 4
+ACT_GELU_TANH = 8
+OP_ROWCOL = 0
+OP_NVFP4 = 1
+DEVERR_TIMEOUT = 1
+
+STATUS_NAMES = {0: "MXQ_OK", 1: "MXQ_EINVAL", 2: "MXQ_ESHAPE", 3: "MXQ_EALIGN",
+                4: "MXQ_EARCH", 5: "MXQ_EWORKSPACE", 6: "MXQ_ECUDA"}
+
+
+class MxqError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _lib.lib().mxq_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def library_path():
+    return _lib.LIB_PATH
+
+
+def _check(status, where):
+    if status != 0:
+        raise MxqError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _input(x, name="x"):
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D torch.bfloat16 tensor")
+    if not x.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if x.size(1) > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} needs a unit column stride")
+    return x.stride(0) if x.size(0) > 1 else x.size(1)
+
+
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def mxq_workspace_bytes(op, M, K, flags):
+    return int(_lib.lib().mxq_workspace_bytes(op, M, K, flags))
+
+
+def mx_quantize_rowcol(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_col=None,
+                       s_col=None, dbias=None, workspace=None, dev_err=None, stream=None):
+    """bf16 x[M, K] -> MXFP8.  Returns a dict with q_row [M,K] / s_row
+    [M,K/32] (ROWWISE), q_col [K,M] / s_col [K,M/32] (COLWISE), dbias [K]
+    fp32 (DBIAS); codes and scales are torch.uint8."""
+    ldx = _input(x)
+    M, K = x.shape
+    dev = x.device
+    out = {}
+    if flags & ROWWISE:
+        out["q_row"] = q_row if q_row is not None else _empty((M, K), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty((M, K // 32), torch.uint8, dev)
+    if flags & COLWISE:
+        out["q_col"] = q_col if q_col is not None else _empty((K, M), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty((K, M // 32), torch.uint8, dev)
+    ws_bytes = 0
+    if flags & DBIAS:
+        out["dbias"] = dbias if dbias is not None else _empty((K,), torch.float32, dev)
+        if workspace is None:
+            need = mxq_workspace_bytes(OP_ROWCOL, M, K, flags)
+            workspace = _empty((max(need, 16),), torch.uint8, dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = _lib.lib().mx_quantize_rowcol(
+        _ptr(x), M, K, ldx, flags, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
+        _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(out.get("dbias")),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    _check(st, "mx_quantize_rowcol")
+    return out
+
+
+def mx_quantize_gated(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_col=None,
+                      s_col=None, dev_err=None, stream=None):
+    """SwiGLU-gated MXFP8 of x[M, 2N] = [gate | up]; y = silu(gate) * up
+    in fp32, quantized like mx_quantize_rowcol (outputs sized by N)."""
+    ldx = _input(x)
+    M, W = x.shape
+    if W % 2:
+        raise ValueError("x must hold [gate | up] halves of equal width")
+    N = W // 2
+    dev = x.device
+    out = {}
+    if flags & ROWWISE:
+        out["q_row"] = q_row if q_row is not None else _empty((M, N), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty((M, N // 32), torch.uint8, dev)
+    if flags & COLWISE:
+        out["q_col"] = q_col if q_col is not None else _empty((N, M), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty((N, M // 32), torch.uint8, dev)
+    st = _lib.lib().mx_quantize_gated(
+        _ptr(x), M, N, ldx, flags, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
+        _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(dev_err), _stream(stream))
+    _check(st, "mx_quantize_gated")
+    return out
+
+
+def bf16_amax(x, *, out=None, stream=None):
+    """Largest |x| as a 1-element fp32 device tensor."""
+    ldx = _input(x)
+    M, K = x.shape
+    if out is None:
+        out = _empty((1,), torch.float32, x.device)
+    st = _lib.lib().bf16_amax(_ptr(x), M, K, ldx, _ptr(out), _stream(stream))
+    _check(st, "bf16_amax")
+    return out
+
+
+def nvfp4_quantize_transpose(x, flags=ROWWISE | COLWISE, *, amax=None, global_scale=None,
+                             q_row=None, s_row=None, q_t=None, s_t=None, workspace=None,
+                             dev_err=None, stream=None):
+    """bf16 x[M, K] -> NVFP4: q_row [M,K/2] / s_row [M,K/16] (ROWWISE),
+    q_t [K,M/2] / s_t [K,M/16] (COLWISE), global_scale [1] fp32.  `amax`
+    (1-element fp32 device tensor) skips the internal amax pass."""
+    ldx = _input(x)
+    M, K = x.shape
+    dev = x.device
+    out = {"global_scale": global_scale if global_scale is not None
+           else _empty((1,), torch.float32, dev)}
+    if flags & ROWWISE:
+        out["q_row"] = q_row if q_row is not None else _empty((M, K // 2), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty((M, K // 16), torch.uint8, dev)
+    if flags & COLWISE:
+        out["q_t"] = q_t if q_t is not None else _empty((K, M // 2), torch.uint8, dev)
+        out["s_t"] = s_t if s_t is not None else _empty((K, M // 16), torch.uint8, dev)
+    ws_bytes = 0
+    if amax is None:
+        if workspace is None:
+            workspace = _empty((16,), torch.uint8, dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = _lib.lib().nvfp4_quantize_transpose(
+        _ptr(x), M, K, ldx, flags, _ptr(amax), _ptr(out["global_scale"]),
+        _ptr(out.get("q_row")), _ptr(out.get("s_row")), _ptr(out.get("q_t")),
+        _ptr(out.get("s_t")), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    _check(st, "nvfp4_quantize_transpose")
+    return out
+
+
+def mxq_selftest_bounded_wait(timeout_ns, dev_err, *, stream=None):
+    """Run the bounded-wait self test (see include/mxq.h); the kernel sets
+    DEVERR_TIMEOUT in dev_err (a 1-element int32 device tensor)."""
+    st = _lib.lib().mxq_selftest_bounded_wait(int(timeout_ns), _ptr(dev_err), _stream(stream))
+    _check(st, "mxq_selftest_bounded_wait")

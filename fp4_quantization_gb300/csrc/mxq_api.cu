@@ -1,0 +1,299 @@
+// mxq_api.cu -- the extern "C" entry points declared in include/mxq.h:
+// argument validation, device checks, TMA descriptor encoding and dispatch
+// to the kernels.  Host code only; it allocates nothing and never
+// synchronises.
+
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mxq.h"
+#include "mxq_internal.h"
+
+namespace {
+
+using mxq::DEFAULT_TIMEOUT_NS;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int checked = 0;     // 0 unknown, 1 sm_103, -1 other
+  int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+// Looks up (once per device) whether the current device is sm_103 and how
+// many SMs it has.
+mxq_status current_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXQ_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MXQ_EARCH;
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (d.checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MXQ_ECUDA;
+    d.checked = (major == 10 && minor == 3) ? 1 : -1;
+    d.num_sms = sms;
+  }
+  if (d.checked < 0) return MXQ_EARCH;
+  *num_sms = d.num_sms;
+  return MXQ_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Encodes a 2-D bf16 tensor map over x[rows][cols] (row stride ldx
+// elements) with a box of box_cols x box_rows; out-of-range reads give 0.
+mxq_status encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols,
+                           int64_t ldx, int box_cols, int box_rows) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return MXQ_ECUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims,
+                              strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MXQ_OK : MXQ_ECUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+mxq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA; }
+
+// Shared checks of the MXFP8 entry points; `width` is the quantized width.
+mxq_status check_mx_outputs(uint32_t flags, int64_t width, const uint8_t* q_row,
+                            const uint8_t* s_row, const uint8_t* q_col, const uint8_t* s_col) {
+  (void)width;
+  if ((flags & MXQ_ROWWISE) && (!q_row || !s_row)) return MXQ_EINVAL;
+  if ((flags & MXQ_COLWISE) && (!q_col || !s_col)) return MXQ_EINVAL;
+  if ((flags & MXQ_ROWWISE) && (!aligned(q_row, 16) || !aligned(s_row, 16))) return MXQ_EALIGN;
+  if ((flags & MXQ_COLWISE) && (!aligned(q_col, 16) || !aligned(s_col, 16))) return MXQ_EALIGN;
+  return MXQ_OK;
+}
+
+int direction_mode(uint32_t flags) {
+  return ((flags & MXQ_ROWWISE) ? mxq::MX_ROW : 0) | ((flags & MXQ_COLWISE) ? mxq::MX_COL : 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mxq_status_string(int status) {
+  switch (status) {
+    case MXQ_OK: return "MXQ_OK";
+    case MXQ_EINVAL: return "MXQ_EINVAL: null pointer or bad flags";
+    case MXQ_ESHAPE: return "MXQ_ESHAPE: bad matrix shape";
+    case MXQ_EALIGN: return "MXQ_EALIGN: misaligned pointer or stride";
+    case MXQ_EARCH: return "MXQ_EARCH: device is not sm_103";
+    case MXQ_EWORKSPACE: return "MXQ_EWORKSPACE: workspace missing or too small";
+    case MXQ_ECUDA: return "MXQ_ECUDA: CUDA error";
+    default: return "unknown mxq status";
+  }
+}
+
+size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags) {
+  if (M <= 0 || K <= 0) return 0;
+  if (op == MXQ_OP_NVFP4) return 16;   // one fp32 amax, padded
+  if (op != MXQ_OP_ROWCOL || !(flags & MXQ_DBIAS)) return 0;
+  int sms = 0;
+  if (current_device(&sms) != MXQ_OK) return 0;
+  const int tiles_m = static_cast<int>(M / mxq::MX_TILE_M);
+  const int tiles_k = static_cast<int>((K + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
+  const int groups = mxq::mx_dbias_groups(tiles_m, tiles_k, sms);
+  return static_cast<size_t>(groups) * static_cast<size_t>(K) * sizeof(float);
+}
+
+mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t flags,
+                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                              float* dbias, void* workspace, size_t workspace_bytes,
+                              uint32_t* dev_err, mxq_stream_t stream) {
+  const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH;
+  if (flags & ~known) return MXQ_EINVAL;
+  if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
+  if ((flags & MXQ_DBIAS) && (flags & MXQ_ACT_GELU_TANH)) return MXQ_EINVAL;
+  if (M < 0 || K < 0 || ldx < K) return MXQ_ESHAPE;
+  if ((M % 32) || (K % 32)) return MXQ_ESHAPE;
+  if (M > (int64_t(1) << 30) || K > (int64_t(1) << 30) || M * K > (int64_t(1) << 40))
+    return MXQ_ESHAPE;
+  const bool want_dbias = (flags & MXQ_DBIAS) != 0;
+  if (want_dbias && !dbias) return MXQ_EINVAL;
+  if (want_dbias && !aligned(dbias, 16)) return MXQ_EALIGN;
+  int sms = 0;
+  mxq_status st = current_device(&sms);
+  if (st != MXQ_OK) return st;
+  if (M == 0 || K == 0) {
+    if (want_dbias && K > 0)
+      return from_cuda(cudaMemsetAsync(dbias, 0, static_cast<size_t>(K) * sizeof(float), stream));
+    return MXQ_OK;
+  }
+  if (!x) return MXQ_EINVAL;
+  if (!aligned(x, 16) || (ldx % 8)) return MXQ_EALIGN;
+  st = check_mx_outputs(flags, K, q_row, s_row, q_col, s_col);
+  if (st != MXQ_OK) return st;
+
+  mxq::MxArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.tiles_m = static_cast<int>(M / mxq::MX_TILE_M);
+  a.tiles_k = static_cast<int>((K + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_col = q_col;
+  a.s_col = s_col;
+  a.dev_err = dev_err;
+  a.timeout_ns = DEFAULT_TIMEOUT_NS;
+  if (want_dbias) {
+    a.dbias_groups = mxq::mx_dbias_groups(a.tiles_m, a.tiles_k, sms);
+    const size_t need = static_cast<size_t>(a.dbias_groups) * static_cast<size_t>(K) * sizeof(float);
+    if (!workspace || workspace_bytes < need) return MXQ_EWORKSPACE;
+    if (!aligned(workspace, 16)) return MXQ_EALIGN;
+    a.dbias_ws = static_cast<float*>(workspace);
+  }
+  CUtensorMap map;
+  st = encode_bf16_map(&map, x, M, K, ldx, mxq::MX_TILE_K, mxq::MX_TILE_M);
+  if (st != MXQ_OK) return st;
+  const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_GELU : mxq::ACT_NONE;
+  st = from_cuda(mxq::launch_mx(map, a, direction_mode(flags), want_dbias, act, sms, stream));
+  if (st != MXQ_OK || !want_dbias) return st;
+  return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.dbias_groups, a.K, dbias, stream));
+}
+
+mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, uint32_t flags,
+                             uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                             uint32_t* dev_err, mxq_stream_t stream) {
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE)) return MXQ_EINVAL;
+  if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
+  if (M < 0 || N < 0 || ldx < 2 * N) return MXQ_ESHAPE;
+  if ((M % 32) || (N % 32)) return MXQ_ESHAPE;
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 29) || M * N > (int64_t(1) << 40))
+    return MXQ_ESHAPE;
+  int sms = 0;
+  mxq_status st = current_device(&sms);
+  if (st != MXQ_OK) return st;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!x) return MXQ_EINVAL;
+  if (!aligned(x, 16) || (ldx % 8)) return MXQ_EALIGN;
+  st = check_mx_outputs(flags, N, q_row, s_row, q_col, s_col);
+  if (st != MXQ_OK) return st;
+
+  mxq::MxArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(N);
+  a.tiles_m = static_cast<int>(M / mxq::MX_TILE_M);
+  a.tiles_k = static_cast<int>((N + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
+  a.up_col = static_cast<int>(N);
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_col = q_col;
+  a.s_col = s_col;
+  a.dev_err = dev_err;
+  a.timeout_ns = DEFAULT_TIMEOUT_NS;
+  CUtensorMap map;
+  // The map spans [gate | up]; gate boxes start at column k, up boxes at N + k.
+  st = encode_bf16_map(&map, x, M, 2 * N, ldx, mxq::MX_TILE_K, mxq::MX_TILE_M);
+  if (st != MXQ_OK) return st;
+  return from_cuda(mxq::launch_mx(map, a, direction_mode(flags), false, mxq::ACT_SWIGLU, sms, stream));
+}
+
+mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* amax_out,
+                     mxq_stream_t stream) {
+  if (!amax_out) return MXQ_EINVAL;
+  if (M < 0 || K < 0 || ldx < K) return MXQ_ESHAPE;
+  if (K % 8) return MXQ_ESHAPE;
+  if (!aligned(amax_out, 4)) return MXQ_EALIGN;
+  int sms = 0;
+  mxq_status st = current_device(&sms);
+  if (st != MXQ_OK) return st;
+  if (M > 0 && K > 0) {
+    if (!x) return MXQ_EINVAL;
+    if (!aligned(x, 16) || (ldx % 8)) return MXQ_EALIGN;
+  }
+  return from_cuda(mxq::launch_bf16_amax(x, M, K, ldx, amax_out, sms, stream));
+}
+
+mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                    uint32_t flags, const float* amax_in, float* global_scale,
+                                    uint8_t* q_row, uint8_t* s_row, uint8_t* q_t, uint8_t* s_t,
+                                    void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                                    mxq_stream_t stream) {
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE)) return MXQ_EINVAL;
+  if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
+  if (M < 0 || K < 0 || ldx < K) return MXQ_ESHAPE;
+  if ((M % 16) || (K % 16)) return MXQ_ESHAPE;
+  if (M > (int64_t(1) << 30) || K > (int64_t(1) << 30) || M * K > (int64_t(1) << 40))
+    return MXQ_ESHAPE;
+  if (!global_scale) return MXQ_EINVAL;
+  if (!aligned(global_scale, 4)) return MXQ_EALIGN;
+  int sms = 0;
+  mxq_status st = current_device(&sms);
+  if (st != MXQ_OK) return st;
+  if (M == 0 || K == 0) {
+    // Nothing to quantize; G = amax / 2688 from the caller's amax, else 0.
+    if (!amax_in) return from_cuda(cudaMemsetAsync(global_scale, 0, sizeof(float), stream));
+    return from_cuda(mxq::launch_nv_global_scale(amax_in, global_scale, stream));
+  }
+  const float* amax = amax_in;
+  if (!amax) {
+    if (!workspace || workspace_bytes < sizeof(float)) return MXQ_EWORKSPACE;
+    if (!aligned(workspace, 16)) return MXQ_EALIGN;
+  }
+  if (!x) return MXQ_EINVAL;
+  if (!aligned(x, 16) || (ldx % 8)) return MXQ_EALIGN;
+  if ((flags & MXQ_ROWWISE) && (!q_row || !s_row)) return MXQ_EINVAL;
+  if ((flags & MXQ_COLWISE) && (!q_t || !s_t)) return MXQ_EINVAL;
+  if ((flags & MXQ_ROWWISE) && (!aligned(q_row, 16) || !aligned(s_row, 16))) return MXQ_EALIGN;
+  if ((flags & MXQ_COLWISE) && (!aligned(q_t, 16) || !aligned(s_t, 16))) return MXQ_EALIGN;
+
+  if (!amax) {
+    float* ws_amax = static_cast<float*>(workspace);
+    st = from_cuda(mxq::launch_bf16_amax(x, M, K, ldx, ws_amax, sms, stream));
+    if (st != MXQ_OK) return st;
+    amax = ws_amax;
+  }
+  mxq::NvArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.tiles_m = static_cast<int>((M + mxq::NV_TILE_M - 1) / mxq::NV_TILE_M);
+  a.tiles_k = static_cast<int>((K + mxq::NV_TILE_K - 1) / mxq::NV_TILE_K);
+  a.amax = amax;
+  a.global_scale = global_scale;
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_t = q_t;
+  a.s_t = s_t;
+  a.dev_err = dev_err;
+  a.timeout_ns = DEFAULT_TIMEOUT_NS;
+  CUtensorMap map;
+  st = encode_bf16_map(&map, x, M, K, ldx, mxq::NV_TILE_K, mxq::NV_TILE_M);
+  if (st != MXQ_OK) return st;
+  return from_cuda(mxq::launch_nvfp4(map, a, direction_mode(flags), sms, stream));
+}
+
+mxq_status mxq_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* dev_err, mxq_stream_t stream) {
+  if (!dev_err) return MXQ_EINVAL;
+  if (timeout_ns < 1000ull || timeout_ns > 5000000000ull) return MXQ_EINVAL;
+  int sms = 0;
+  mxq_status st = current_device(&sms);
+  if (st != MXQ_OK) return st;
+  return from_cuda(mxq::launch_selftest_wait(timeout_ns, dev_err, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// mxq_internal.h -- launch arguments and launchers shared between the kernel
+// translation units and the C ABI layer (mxq_api.cu).  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mxq {
+
+// MXFP8 warp tile: 32 rows (one colwise block) x 128 columns (four rowwise
+// blocks) of bf16 = 8 KiB, loaded by one TMA box.
+constexpr int MX_TILE_M = 32;
+constexpr int MX_TILE_K = 128;
+
+// NVFP4 warp tile: 64 x 64 bf16 = 8 KiB (four 16-row transposed blocks per
+// column, four 1x16 row blocks per row).
+constexpr int NV_TILE_M = 64;
+constexpr int NV_TILE_K = 64;
+
+constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000000000ull;   // 1 s per wait
+
+enum : int { MX_ROW = 1, MX_COL = 2 };
+enum : int { ACT_NONE = 0, ACT_GELU = 1, ACT_SWIGLU = 2 };
+
+struct MxArgs {
+  int M, K;                 // shape of y (the quantized matrix)
+  int tiles_m, tiles_k;     // MX_TILE_M x MX_TILE_K tiles covering y
+  int up_col;               // SwiGLU: column of the up half in x; else 0
+  int dbias_groups;         // row groups of the dbias schedule, 0 without dbias
+  uint8_t* q_row;
+  uint8_t* s_row;
+  uint8_t* q_col;
+  uint8_t* s_col;
+  float* dbias_ws;          // [dbias_groups][K] partial column sums
+  uint32_t* dev_err;
+  uint64_t timeout_ns;
+};
+
+struct NvArgs {
+  int M, K;
+  int tiles_m, tiles_k;     // NV_TILE_M x NV_TILE_K tiles
+  const float* amax;        // device tensor amax
+  float* global_scale;      // device, receives amax / 2688
+  uint8_t* q_row;
+  uint8_t* s_row;
+  uint8_t* q_t;
+  uint8_t* s_t;
+  uint32_t* dev_err;
+  uint64_t timeout_ns;
+};
+
+// Number of row groups the dbias schedule uses on a device with `num_sms`
+// SMs (each group's partial sums take K floats of workspace).
+int mx_dbias_groups(int tiles_m, int tiles_k, int num_sms);
+
+cudaError_t launch_mx(const CUtensorMap& map, const MxArgs& a, int mode, bool dbias, int act,
+                      int num_sms, cudaStream_t stream);
+cudaError_t launch_dbias_finalize(const float* ws, int groups, int K, float* dbias,
+                                  cudaStream_t stream);
+cudaError_t launch_nvfp4(const CUtensorMap& map, const NvArgs& a, int mode, int num_sms,
+                         cudaStream_t stream);
+cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,
+                             int num_sms, cudaStream_t stream);
+cudaError_t launch_nv_global_scale(const float* amax, float* global_scale, cudaStream_t stream);
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, uint32_t* dev_err, cudaStream_t stream);
+
+}  // namespace mxq

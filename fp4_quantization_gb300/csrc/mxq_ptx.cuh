@@ -1,0 +1,207 @@
+// mxq_ptx.cuh -- sm_103a device helpers for the quantization kernels:
+// shared-memory addressing, mbarriers with bounded waits, TMA tile loads,
+// packed-integer max, and the hardware FP8 / FP4 conversions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace mxq {
+
+// ---------------------------------------------------------------------------
+// Shared memory addressing
+// ---------------------------------------------------------------------------
+
+// Rounds a dynamic-shared-memory pointer up to ALIGN bytes by adding the pad
+// to the original pointer.  Going through an integer and back would lose the
+// pointer's tie to the __shared__ object and make the compiler fall back to
+// generic loads and stores (TE PR #3291 "Fix pointer arithmatic to generate
+// correct LDS/STS instructions", description).
+template <int ALIGN, typename T>
+__device__ __forceinline__ T* align_up_shared(T* p) {
+  static_assert((ALIGN & (ALIGN - 1)) == 0, "power of two");
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  const uint32_t pad = (ALIGN - (s & (ALIGN - 1))) & (ALIGN - 1);
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(p) + pad);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts8(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Global stores (outputs are written once and not re-read by this kernel)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void stg64(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.b32 [%0], {%1, %2};" :: "l"(p), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void stg32(void* p, uint32_t a) {
+  asm volatile("st.global.b32 [%0], %1;" :: "l"(p), "r"(a) : "memory");
+}
+
+__device__ __forceinline__ void stg8(void* p, uint32_t a) {
+  asm volatile("st.global.u8 [%0], %1;" :: "l"(p), "r"(a) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + TMA
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the TMA unit (async proxy).
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits until the barrier phase with `parity` has completed, or until
+// `timeout_ns` nanoseconds have passed.  Returns false on timeout.  Every
+// wait in this library goes through here, so no kernel can spin forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// 2-D TMA tile load global -> shared, completing `bytes` on `bar`.
+// x is the innermost (column) coordinate in elements, y the row.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Packed integer helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// bf16 halves of a packed pair, widened exactly to fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// Conversions
+// ---------------------------------------------------------------------------
+
+// Two fp32 -> two E4M3 (round to nearest even, saturating to +-448); `lo`
+// lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return static_cast<uint32_t>(r);
+}
+
+// Four fp32 -> four E4M3 codes packed little-endian (a in the low byte).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
+  return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
+}
+
+// Eight fp32 -> eight E2M1 codes packed little-endian, two per byte, element
+// 2i in the low nibble of byte i (round to nearest even, saturating to +-6).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, float v3,
+                                               float v4, float v5, float v6, float v7) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return out;
+}
+
+// One E4M3 code -> its exact fp32 value.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(code & 0xFF);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFF)));
+}
+
+// Shared-scale (E8M0) code of an MX block from the fp32/bf16 exponent field
+// E of its largest magnitude: max(0, E - 8).  The block's elements are then
+// multiplied by 2^(127 - code), whose fp32 bit pattern is (254 - code) << 23.
+__device__ __forceinline__ uint32_t e8m0_from_exponent(uint32_t E) { return E > 8u ? E - 8u : 0u; }
+__device__ __forceinline__ float inv_scale_from_e8m0(uint32_t code) {
+  return __uint_as_float((254u - code) << 23);
+}
+
+}  // namespace mxq

@@ -1,0 +1,188 @@
+/*
+ * mxq.h -- C ABI of libmxq, GB300 (sm_103a) block-scaled quantization.
+ *
+ * The library turns a bf16 matrix into OCP-MX MXFP8 (E4M3 codes, one E8M0
+ * scale per 32-element block) rowwise and colwise from a single HBM read,
+ * optionally fused with a dbias column sum, a tanh-GELU or a SwiGLU gate, and
+ * into NVFP4 (E2M1 codes, one E4M3 scale per 16 elements, one fp32 tensor
+ * scale) rowwise and transposed.
+ *
+ * Kernel families this covers (TransformerEngine PR #3291 "Fix pointer
+ * arithmatic to generate correct LDS/STS instructions", results tables
+ * "MXFP8 generic quantize kernel", "MXFP8 specialized cast-only kernel
+ * (bidimensional)", "MXFP8 gated (swiglu / geglu) kernel" and "NVFP4 2D
+ * quantize-transpose kernel"; the colwise-only cast is the "dim1" cast of
+ * torchao PR #12 "Multiply with inverse scale in loop instead of dividing",
+ * section "Performance").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * All pointers are DEVICE pointers unless stated otherwise; the caller
+ *    owns every buffer.  The library never allocates, frees or synchronises:
+ *    all work is enqueued on `stream` (NULL = the legacy default stream), and
+ *    every buffer must stay valid until the stream has passed this call.
+ *  * Matrices are row-major.  `x` is bf16 (raw 16-bit patterns) with a row
+ *    stride of `ldx` elements; outputs are dense (row stride = width).
+ *  * Host-checkable problems return a status synchronously and enqueue
+ *    nothing.  A launch failure returns MXQ_ECUDA.
+ *  * `dev_err` (optional, device, 4 bytes): every wait inside the kernels is
+ *    bounded; if one runs out, the kernel ORs MXQ_DEVERR_TIMEOUT into
+ *    *dev_err, waits (bounded) for its own copies in flight and exits
+ *    without writing the remaining tiles.  The library never clears
+ *    *dev_err; the caller zeroes it and reads it back after the stream.
+ *  * Alignment: `x`, every output and the workspace 16-byte aligned, `ldx`
+ *    a multiple of 8.  Violations return MXQ_EALIGN.
+ *  * The device must be compute capability 10.3 (GB300): else MXQ_EARCH.
+ *  * NaN or infinite inputs are outside the contract.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MXQ_API __attribute__((visibility("default")))
+#else
+#define MXQ_API
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* mxq_stream_t;
+
+typedef enum {
+    MXQ_OK = 0,
+    MXQ_EINVAL = 1,      /* NULL pointer, bad flag combination            */
+    MXQ_ESHAPE = 2,      /* negative size or size not a block multiple    */
+    MXQ_EALIGN = 3,      /* pointer or stride misaligned                  */
+    MXQ_EARCH = 4,       /* current device is not sm_103                  */
+    MXQ_EWORKSPACE = 5,  /* workspace missing or too small                */
+    MXQ_ECUDA = 6        /* CUDA runtime error while launching            */
+} mxq_status;
+
+/* flags */
+enum {
+    MXQ_ROWWISE = 1,        /* 1x32 (MX) / 1x16 (NVFP4) blocks along K     */
+    MXQ_COLWISE = 2,        /* 32x1 (MX) / 16x1 (NVFP4) blocks along M,    */
+                            /* stored transposed: [K][M]                   */
+    MXQ_DBIAS = 4,          /* fp32 column sums of x (mx_quantize_rowcol)  */
+    MXQ_ACT_GELU_TANH = 8   /* quantize gelu_tanh(x) (mx_quantize_rowcol)  */
+};
+
+/* bits of *dev_err */
+enum { MXQ_DEVERR_TIMEOUT = 1 };
+
+/* operation ids for mxq_workspace_bytes */
+enum { MXQ_OP_ROWCOL = 0, MXQ_OP_NVFP4 = 1 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+MXQ_API const char* mxq_status_string(int status);
+
+/* Workspace bytes `op` needs for an M x K input with `flags` on the current
+ * device (0 when none is needed).  MXQ_OP_ROWCOL needs one only with
+ * MXQ_DBIAS; MXQ_OP_NVFP4 needs 4 bytes when no amax_in is given. */
+MXQ_API size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags);
+
+/*
+ * mx_quantize_rowcol -- bf16 -> MXFP8 rowwise and/or colwise, one HBM read.
+ *
+ * Operation (per 32-value block B of y, y = x, or y = gelu_tanh(x) in fp32
+ * with MXQ_ACT_GELU_TANH, gelu_tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi)
+ * (x + 0.044715 x^3)))):  a = max|y| over B;  e = floor(log2 a) - 8 clamped
+ * to [-127, 127] (a = 0 -> scale code 0);  scale code = e + 127 (E8M0);
+ * codes = E4M3(y * 2^-e), round-to-nearest-even, saturating to +-448.  The
+ * multiply by the exact power of two 2^-e replaces a per-element division
+ * (torchao PR #12, rationale section).  Rowwise blocks are 1x32 along K,
+ * colwise blocks 32x1 along M (TE PR #3291 tables, dir "row"/"col"/"both").
+ * MXQ_DBIAS adds dbias[k] = sum_m x[m][k] in fp32 (TE PR #3291 fusion
+ * "dbias"; not combinable with MXQ_ACT_GELU_TANH).
+ *
+ *   x       [M][ldx] bf16, M % 32 == 0, K % 32 == 0, ldx >= K.
+ *   flags   MXQ_ROWWISE | MXQ_COLWISE (at least one), optional MXQ_DBIAS or
+ *           MXQ_ACT_GELU_TANH.
+ *   q_row   [M][K] E4M3 codes, s_row [M][K/32] E8M0 (needed with ROWWISE,
+ *           else ignored).
+ *   q_col   [K][M] E4M3 codes (row k holds column k of the blocks),
+ *           s_col [K][M/32] E8M0 (needed with COLWISE, else ignored).
+ *   dbias   [K] fp32 (needed with MXQ_DBIAS).
+ *   workspace / workspace_bytes: device scratch of at least
+ *           mxq_workspace_bytes(MXQ_OP_ROWCOL, M, K, flags) bytes, 16-byte
+ *           aligned (dbias partial sums); may be NULL when that is 0.
+ *   M == 0 or K == 0 is a valid empty call (dbias is zero-filled).
+ */
+MXQ_API mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t flags,
+                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                              float* dbias, void* workspace, size_t workspace_bytes,
+                              uint32_t* dev_err, mxq_stream_t stream);
+
+/*
+ * mx_quantize_gated -- SwiGLU gate fused with MXFP8 quantization.
+ *
+ * Operation: y[m][n] = silu(x[m][n]) * x[m][N + n] for n < N, silu(g) =
+ * g / (1 + e^-g), computed in fp32 (no intermediate bf16 rounding), then
+ * quantized exactly as mx_quantize_rowcol quantizes y (TE PR #3291 table
+ * "MXFP8 gated (swiglu / geglu) kernel", fusion "swiglu").
+ *
+ *   x       [M][ldx] bf16 holding [gate | up], each N wide; ldx >= 2N.
+ *   M % 32 == 0, N % 32 == 0.
+ *   q_row [M][N], s_row [M][N/32], q_col [N][M], s_col [N][M/32] as above.
+ */
+MXQ_API mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, uint32_t flags,
+                             uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                             uint32_t* dev_err, mxq_stream_t stream);
+
+/*
+ * bf16_amax -- largest |x| of a bf16 matrix, written as fp32 to *amax_out
+ * (device).  The exact maximum, so the result does not depend on the order
+ * of the reduction.  Needed for the NVFP4 tensor scale.
+ *   x [M][ldx], K % 8 == 0.  M == 0 or K == 0 writes 0.
+ */
+MXQ_API mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* amax_out,
+                     mxq_stream_t stream);
+
+/*
+ * nvfp4_quantize_transpose -- bf16 -> NVFP4, rowwise and transposed.
+ *
+ * Operation (TE PR #3291, "NVFP4 quantize-transpose" family, 1D variant;
+ * every step one fp32 IEEE operation in this order):
+ *   A = tensor amax (from amax_in, else from an internal bf16_amax pass);
+ *   G = A / 2688 (2688 = 448 * 6), written to *global_scale;
+ *   per block of 16 values (1x16 along K rowwise; 16x1 along M for the
+ *   transposed output): b = block amax; s = E4M3((b / 6) / G) (RNE,
+ *   saturating); d = value(s) * G; inv = 1 / d (0 when s == 0 or d == 0,
+ *   the largest finite float if 1 / d overflows);
+ *   codes = E2M1(x * inv), round-to-nearest-even, saturating to +-6,
+ *   packed two per byte, element 2i in the low nibble.  A == 0 gives
+ *   G = 0 and all-zero scales.
+ *
+ *   x       [M][ldx] bf16, M % 16 == 0, K % 16 == 0.
+ *   flags   MXQ_ROWWISE and/or MXQ_COLWISE (= the transposed output).
+ *   amax_in device fp32 tensor amax, or NULL to compute it here (then the
+ *           workspace must hold 4 bytes).
+ *   global_scale  device fp32, receives G (required).
+ *   q_row [M][K/2], s_row [M][K/16] (E4M3); q_t [K][M/2], s_t [K][M/16].
+ */
+MXQ_API mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                    uint32_t flags, const float* amax_in, float* global_scale,
+                                    uint8_t* q_row, uint8_t* s_row, uint8_t* q_t, uint8_t* s_t,
+                                    void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                                    mxq_stream_t stream);
+
+/*
+ * mxq_selftest_bounded_wait -- launches one warp that waits on a barrier
+ * nothing will ever complete, through the same bounded-wait routine the
+ * quantization kernels use, with a limit of `timeout_ns` nanoseconds
+ * (1e3..5e9).  The kernel ORs MXQ_DEVERR_TIMEOUT into *dev_err (required)
+ * and returns, leaving the context usable.  Lets a test check the timeout
+ * path without faulting or hanging a GPU.
+ */
+MXQ_API mxq_status mxq_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* dev_err, mxq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXQ_H */

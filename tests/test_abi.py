@@ -1,0 +1,83 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every
+function include/mxq.h declares with the signature the binding uses, and
+rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import fp4_quantization_gb300 as mxq
+from fp4_quantization_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxq.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"MXQ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for required in ("mx_quantize_rowcol", "mx_quantize_gated", "nvfp4_quantize_transpose",
+                     "bf16_amax"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = _lib.lib()
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for name in names:
+        assert hasattr(L, name), name
+    # The binding's signature table covers exactly the declared functions.
+    assert set(_lib.SIGNATURES) == set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+
+
+def test_status_strings():
+    L = _lib.lib()
+    for code, name in mxq.STATUS_NAMES.items():
+        assert L.mxq_status_string(code).decode().startswith(name)
+    assert L.mxq_status_string(99) == b"unknown mxq status"
+
+
+def _rowcol(**kw):
+    args = dict(x=None, M=64, K=64, ldx=64, flags=3, q_row=None, s_row=None, q_col=None,
+                s_col=None, dbias=None, ws=None, ws_bytes=0, err=None, stream=None)
+    args.update(kw)
+    return _lib.lib().mx_quantize_rowcol(*args.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=0), 1),                    # no direction
+    (dict(flags=16 | 1), 1),               # unknown flag bit
+    (dict(flags=1 | 4 | 8), 1),            # dbias with gelu
+    (dict(M=-32), 2),
+    (dict(M=48), 2),                       # not a multiple of 32
+    (dict(K=40, ldx=40), 2),
+    (dict(ldx=32), 2),                     # ldx < K
+])
+def test_rowcol_host_validation(kw, status):
+    assert _rowcol(**kw) == status
+
+
+def test_gated_and_nvfp4_host_validation():
+    L = _lib.lib()
+    assert L.mx_quantize_gated(None, 64, 64, 100, 3, None, None, None, None, None, None) == 2
+    assert L.mx_quantize_gated(None, 64, 48, 96, 3, None, None, None, None, None, None) == 2
+    assert L.mx_quantize_gated(None, 64, 64, 128, 4, None, None, None, None, None, None) == 1
+    nv = L.nvfp4_quantize_transpose
+    assert nv(None, 24, 32, 32, 3, None, None, None, None, None, None, None, 0, None, None) == 2
+    assert nv(None, 32, 32, 32, 0, None, None, None, None, None, None, None, 0, None, None) == 1
+    assert nv(None, 32, 32, 32, 3, None, None, None, None, None, None, None, 0, None, None) == 1
+    assert L.bf16_amax(None, 16, 12, 12, None, None) == 1
+    assert L.bf16_amax(None, 16, 12, 12, ctypes.c_void_p(16), None) == 2
+    assert L.mxq_selftest_bounded_wait(10, None, None) == 1

@@ -1,0 +1,206 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, element
+by element, on seeded inputs that span several tiles and a ragged tail.
+
+Bars: plain casts, dbias codes and NVFP4 bit-exact; dbias within 1e-5 of
+sum|x| per column; GELU / SwiGLU codes within one E4M3 step in at most 1e-4
+of the elements (and scales within one code in at most 1e-4 of the blocks).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_util import (assert_equal_bytes, check_activation_blocks, host, to_device)
+
+pytestmark = pytest.mark.gpu
+
+mxq = pytest.importorskip("fp4_quantization_gb300")
+
+BOTH = 3
+
+
+def _rowcol_cases():
+    return [
+        ("plain_small", synth.plain_small(), 0),
+        ("multi_tile_ragged_k", synth.dbias(M=96, K=352, seed=31), 0),
+        ("tall_thin", synth.rowcol(M=640, K=32, seed=32), 0),
+        ("wide_short", synth.dim1(M=32, K=1056, seed=33), 0),
+        ("many_tiles", synth.dbias(M=512, K=1024, seed=34), 0),
+    ]
+
+
+@pytest.mark.parametrize("name,bits,_", _rowcol_cases(), ids=[c[0] for c in _rowcol_cases()])
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+def test_mx_rowcol_bit_exact(name, bits, _, flags):
+    x = to_device(bits)
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mxq.mx_quantize_rowcol(x, flags, dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert dev_err.item() == 0
+    ref = oracle.mx_quantize(bits, flags)
+    for key in ref:
+        assert_equal_bytes(host(out[key]), ref[key], f"{name} {key}")
+
+
+def test_mx_rowcol_strided_input():
+    """ldx > K: a column window of a wider matrix."""
+    full = synth.rowcol(M=128, K=512, seed=35)
+    x = to_device(full)[:, 64:64 + 320]
+    out = mxq.mx_quantize_rowcol(x, BOTH)
+    ref = oracle.mx_quantize(full[:, 64:64 + 320], BOTH)
+    for key in ref:
+        assert_equal_bytes(host(out[key]), ref[key], key)
+
+
+def test_mx_rowcol_repeat_is_deterministic():
+    bits = synth.dbias(M=256, K=384, seed=36)
+    x = to_device(bits)
+    a = mxq.mx_quantize_rowcol(x, BOTH)
+    b = mxq.mx_quantize_rowcol(x, BOTH)
+    for key in a:
+        assert torch.equal(a[key], b[key])
+
+
+def _dbias_tolerance(bits):
+    xv = synth.bf16_bits_to_f32(bits).astype(np.float64)
+    return 1e-5 * np.abs(xv).sum(axis=0) + 1e-30
+
+
+@pytest.mark.parametrize("M,K,seed", [(320, 224, 37), (32, 96, 38), (1024, 640, 39)])
+def test_mx_dbias(M, K, seed):
+    bits = synth.dbias(M=M, K=K, seed=seed)
+    x = to_device(bits)
+    out = mxq.mx_quantize_rowcol(x, BOTH | mxq.DBIAS)
+    ref = oracle.mx_quantize(bits, BOTH | oracle.DBIAS)
+    for key in ("q_row", "s_row", "q_col", "s_col"):
+        assert_equal_bytes(host(out[key]), ref[key], f"dbias {key}")
+    err = np.abs(host(out["dbias"]).astype(np.float64) - ref["dbias"].astype(np.float64))
+    assert np.all(err <= _dbias_tolerance(bits)), f"dbias max err {err.max()}"
+
+
+def test_mx_gelu():
+    bits = synth.gelu(M=256, K=384, seed=40)
+    x = to_device(bits)
+    out = mxq.mx_quantize_rowcol(x, BOTH | mxq.ACT_GELU_TANH)
+    ref = oracle.mx_quantize(bits, BOTH, act=oracle.ACT_GELU_TANH)
+    check_activation_blocks(host(out["q_row"]), host(out["s_row"]), ref["q_row"], ref["s_row"], 1, "gelu row")
+    check_activation_blocks(host(out["q_col"]), host(out["s_col"]), ref["q_col"], ref["s_col"], 1, "gelu col")
+
+
+@pytest.mark.parametrize("M,N,seed", [(256, 352, 41), (64, 128, 42)])
+def test_mx_swiglu(M, N, seed):
+    bits = synth.swiglu(M=M, N=N, seed=seed)
+    x = to_device(bits)
+    out = mxq.mx_quantize_gated(x, BOTH)
+    ref = oracle.mx_quantize_swiglu(bits, N)
+    check_activation_blocks(host(out["q_row"]), host(out["s_row"]), ref["q_row"], ref["s_row"], 1, "swiglu row")
+    check_activation_blocks(host(out["q_col"]), host(out["s_col"]), ref["q_col"], ref["s_col"], 1, "swiglu col")
+
+
+def test_mx_swiglu_row_only_and_col_only():
+    bits = synth.swiglu(M=96, N=160, seed=43)
+    x = to_device(bits)
+    ref = oracle.mx_quantize_swiglu(bits, 160)
+    r = mxq.mx_quantize_gated(x, mxq.ROWWISE)
+    c = mxq.mx_quantize_gated(x, mxq.COLWISE)
+    check_activation_blocks(host(r["q_row"]), host(r["s_row"]), ref["q_row"], ref["s_row"], 1, "row")
+    check_activation_blocks(host(c["q_col"]), host(c["s_col"]), ref["q_col"], ref["s_col"], 1, "col")
+
+
+@pytest.mark.parametrize("M,K,seed", [(208, 176, 44), (16, 16, 45), (64, 64, 46), (512, 320, 47)])
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+def test_nvfp4_bit_exact(M, K, seed, flags):
+    bits = synth.nvfp4(M=M, K=K, seed=seed)
+    x = to_device(bits)
+    out = mxq.nvfp4_quantize_transpose(x, flags)
+    ref = oracle.nvfp4_quantize(bits, flags=flags)
+    assert host(out["global_scale"])[0] == np.float32(ref["global_scale"])
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        if key in ref:
+            assert_equal_bytes(host(out[key]), ref[key], f"nvfp4 {key}")
+
+
+def test_nvfp4_given_amax_and_hand_block():
+    """A caller-supplied amax of 2688 makes the global scale exactly 1."""
+    f = np.zeros((32, 32), np.float32)
+    f[0, :12] = [6, 3, -1.5, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.0, 1]
+    bits = synth.f32_to_bf16_bits(f)
+    x = to_device(bits)
+    amax = torch.tensor([2688.0], dtype=torch.float32, device="cuda")
+    out = mxq.nvfp4_quantize_transpose(x, BOTH, amax=amax)
+    ref = oracle.nvfp4_quantize(bits, tensor_amax=2688.0)
+    assert host(out["global_scale"])[0] == 1.0
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        assert_equal_bytes(host(out[key]), ref[key], key)
+    assert host(out["s_row"])[0, 0] == 0x38
+
+
+def test_nvfp4_zero_tensor():
+    bits = np.zeros((64, 64), np.uint16)
+    bits[3, 5] = 0x8000
+    out = mxq.nvfp4_quantize_transpose(to_device(bits), BOTH)
+    ref = oracle.nvfp4_quantize(bits)
+    assert host(out["global_scale"])[0] == 0.0
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        assert_equal_bytes(host(out[key]), ref[key], key)
+
+
+@pytest.mark.parametrize("M,K", [(96, 256), (1, 8), (333, 72)])
+def test_bf16_amax(M, K):
+    bits = synth.nvfp4(M=max(M, 16), K=max(K, 16), seed=48)[:M, :K].copy()
+    got = host(mxq.bf16_amax(to_device(bits)))[0]
+    assert got == np.float32(oracle.bf16_amax(bits))
+
+
+def test_empty_inputs():
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    out = mxq.mx_quantize_rowcol(x, BOTH | mxq.DBIAS)
+    torch.cuda.synchronize()
+    assert out["q_row"].numel() == 0 and torch.all(out["dbias"] == 0)
+    out = mxq.nvfp4_quantize_transpose(x, BOTH)
+    assert host(out["global_scale"])[0] == 0.0
+    amax = torch.tensor([5376.0], device="cuda")
+    out = mxq.nvfp4_quantize_transpose(x, BOTH, amax=amax)
+    assert host(out["global_scale"])[0] == 2.0
+    assert host(mxq.bf16_amax(x))[0] == 0.0
+
+
+def test_device_side_errors():
+    bits = synth.rowcol(M=64, K=128, seed=49)
+    x = to_device(bits)
+    big = torch.empty(64 * 129, dtype=torch.bfloat16, device="cuda")
+    shifted = big[1:1 + 64 * 128].view(64, 128)            # 2-byte offset: misaligned
+    with pytest.raises(mxq.MxqError) as e:
+        mxq.mx_quantize_rowcol(shifted, BOTH)
+    assert e.value.status == 3
+    with pytest.raises(mxq.MxqError) as e:
+        mxq.mx_quantize_rowcol(x, BOTH | mxq.DBIAS, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 5
+    with pytest.raises(mxq.MxqError) as e:
+        mxq.nvfp4_quantize_transpose(x, BOTH, workspace=torch.empty(0, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 5
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing completes gives up after its limit and reports
+    MXQ_DEVERR_TIMEOUT; the next quantization still runs correctly."""
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mxq.mxq_selftest_bounded_wait(20_000_000, dev_err)    # 20 ms
+    torch.cuda.synchronize()
+    assert dev_err.item() == mxq.DEVERR_TIMEOUT
+    bits = synth.plain_small()
+    out = mxq.mx_quantize_rowcol(to_device(bits), BOTH)
+    ref = oracle.mx_quantize(bits, BOTH)
+    assert_equal_bytes(host(out["q_col"]), ref["q_col"], "after timeout")
+
+
+def test_non_default_stream():
+    bits = synth.rowcol(M=256, K=256, seed=50)
+    x = to_device(bits)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = mxq.mx_quantize_rowcol(x, BOTH)
+    s.synchronize()
+    ref = oracle.mx_quantize(bits, BOTH)
+    assert_equal_bytes(host(out["q_row"]), ref["q_row"], "stream q_row")
