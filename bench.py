@@ -335,7 +335,7 @@ def gpu_arm(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
     peak, peak_kind = measured_peaks()
-    M = K = 16384
+    M, K = args.M, args.K
     bits = synth.rowcol(M=M, K=K)
     x = to_device(bits, device)
     outs = mxq.mx_quantize_rowcol(x, mxq.ROWWISE | mxq.COLWISE)
@@ -363,7 +363,7 @@ def gpu_arm(args):
         "vs_baseline": None,
         "dtype": "bf16->e4m3+e8m0",
         "data": "synthetic: N(0,1) bf16, Philox seed 5",
-        "config": {"workload": "mxfp8_rowwise_colwise_16384x16384", "M": M, "K": K, "block": 32,
+        "config": {"workload": f"mxfp8_rowwise_colwise_{M}x{K}", "M": M, "K": K, "block": 32,
                    "directions": "rowwise+colwise", "parallelism": f"replicas x{world}",
                    "l2": "input 512 MiB > 129 MiB L2: no flush between steps"},
         "clocks": clocks.summary(),
@@ -371,7 +371,7 @@ def gpu_arm(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic("mx_rowcol_16384x16384"),
+                     "traffic": recorded_traffic(f"mx_rowcol_{M}x{K}"),
                      "kernel": "mx_quantize_kernel<rowwise|colwise>",
                      "bytes_per_launch": nbytes},
     }
@@ -453,6 +453,9 @@ def main():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=4096)
+    p.add_argument("--M", type=int, default=16384,
+                   help="rows of the timed cast (16384 for the headline number)")
+    p.add_argument("--K", type=int, default=16384, help="columns of the timed cast")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
