@@ -51,6 +51,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    # Optional -D overrides of the launch configuration (tuning builds).
+    extra += os.environ.get("MXQ_NVCC_DEFINES", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))

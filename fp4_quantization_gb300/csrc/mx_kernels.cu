@@ -7,27 +7,37 @@
 // geglu) kernel": swiglu) and the colwise "dim1" cast of torchao PR #12
 // "Multiply with inverse scale in loop instead of dividing".
 //
-// Design (HBM-bound; no tensor-core work on this path):
-//  * Every warp runs its own TMA pipeline: STAGES shared-memory slots, one
-//    mbarrier each; lane 0 issues a 2-D TMA box of 32 rows x 128 columns
-//    (8 KiB of bf16) per slot.  Warps never wait on each other.
-//  * The grid is persistent (one CTA per SM); warp g takes tiles
-//    g, g + W, g + 2W, ... (W = warps in the grid), or, with dbias, a fixed
-//    column strip and every P-th row tile so its column sums stay in
-//    registers.
-//  * Lane (h, c) = (lane / 16, lane % 16) owns rows 16h..16h+15 and
-//    columns 8c..8c+7 of the tile: 16 conflict-free 16-byte shared loads
-//    (each quarter warp reads one contiguous 128-byte row segment).
-//    Colwise 32x1 amax: in-thread over 16 rows + one xor-16 shuffle.
-//    Rowwise 1x32 amax: in-thread over 8 columns + xor-1 / xor-2 shuffles,
-//    two rows packed per 32-bit register.
-//  * The shared scale is read off the exponent field of the amax and the
-//    elements are multiplied by the exact power of two 2^-e (one multiply
-//    per element, no division; torchao PR #12, rationale), then converted
-//    two at a time by cvt.rn.satfinite.e4m3x2.f32.
-//  * Stores: rowwise codes 8 bytes per lane per row (a half warp writes one
-//    contiguous 128-byte row segment); colwise codes 16 bytes per lane per
-//    column (lanes h = 0, 1 fill one 32-byte sector of the [K][M] output).
+// The path is bound by HBM traffic, and on GB300 the write side costs by
+// the number of L2 write requests rather than by bytes: a 1-byte store costs
+// as much as a 32-byte one.  The kernel is laid out so every output leaves
+// in whole sectors or lines:
+//  * One CTA (WARPS warps, one CTA per SM) walks a contiguous range of
+//    "steps"; a step is a band of BAND rows x 128 columns, loaded by one
+//    TMA box into a 2-slot ring (one mbarrier per slot).  Steps run along K
+//    inside a band, bands one after another.
+//  * Warp w owns rows 32w..32w+31 of the band; lane (h, c) = (lane / 16,
+//    lane % 16) owns rows 16h..16h+15 and columns 8c..8c+7 of those: 16
+//    conflict-free 16-byte shared loads (a quarter warp reads one contiguous
+//    128-byte row segment).  Colwise 32x1 amax: in-thread over 16 rows + one
+//    xor-16 shuffle; rowwise 1x32 amax: in-thread over 8 columns + xor-1 /
+//    xor-2 shuffles, two rows per register.
+//  * The shared scale is read off the exponent field of the amax; elements
+//    are multiplied by the exact power of two 2^-e (two per mul.rn.f32x2, no
+//    division; torchao PR #12, rationale) and converted two at a time by
+//    cvt.rn.satfinite.e4m3x2.f32.
+//  * Rowwise codes go straight to global memory: a half warp writes one full
+//    128-byte line per instruction.
+//  * Colwise codes of the whole band are staged in shared memory and leave
+//    through 3-D TMA stores over the [K][M] output viewed as
+//    [k % 8][k / 8][m] with 128-byte swizzle: every global segment is a full
+//    128-byte line, and the swizzle spreads one shared store instruction
+//    over all banks.
+//  * Rowwise scale bytes of 8 consecutive steps (1024 columns) are gathered
+//    in shared memory and written as one 32-byte sector per row; colwise
+//    scale bytes of a band (BAND / 32 blocks) leave as one run per column.
+//  * dbias: per step, the band's column sums are combined across warps in
+//    shared memory and written once per (band, column); a second small
+//    kernel adds the bands.
 
 #include "mxq_internal.h"
 #include "mxq_ptx.cuh"
@@ -69,224 +79,212 @@ __device__ __forceinline__ float swiglu_f32(float g, float u) {
 }
 
 // ---------------------------------------------------------------------------
-// Tile schedule
+// Small helpers
 // ---------------------------------------------------------------------------
 
-struct Schedule {
-  int count;      // tiles this warp processes
-  int first;      // plain: first linear tile; dbias: first row tile
-  int step;       // plain: warps in the grid; dbias: row groups
-  int strip;      // dbias: fixed column tile; -1 for the plain schedule
-  int tiles_k;
-
-  __device__ void coords(int j, int& tm, int& tk) const {
-    if (strip >= 0) {
-      tm = first + j * step;
-      tk = strip;
-    } else {
-      const int t = first + j * step;
-      tm = t / tiles_k;
-      tk = t - tm * tiles_k;
-    }
-  }
-};
-
-__device__ __forceinline__ Schedule make_schedule(const MxArgs& a, int gw, int warps_in_grid,
-                                                  bool dbias) {
-  Schedule s;
-  s.tiles_k = a.tiles_k;
-  if (dbias) {
-    const int P = a.dbias_groups;
-    const int p = gw / a.tiles_k;
-    s.strip = gw - p * a.tiles_k;
-    s.first = p;
-    s.step = P;
-    s.count = (p < P && p < a.tiles_m) ? (a.tiles_m - p + P - 1) / P : 0;
-  } else {
-    const int total = a.tiles_m * a.tiles_k;
-    s.strip = -1;
-    s.first = gw;
-    s.step = warps_in_grid;
-    s.count = gw < total ? (total - gw + warps_in_grid - 1) / warps_in_grid : 0;
-  }
-  return s;
-}
-
-// ---------------------------------------------------------------------------
-// Shared per-tile arithmetic
-// ---------------------------------------------------------------------------
-
-// Packed exponents (two 16-bit lanes) -> two E8M0 codes (two 16-bit lanes).
+// Packed exponents (two 16-bit lanes) -> two E8M0 codes (two 16-bit lanes):
+// max(E, 8) - 8 on both halves (no borrow crosses halves after the max).
 __device__ __forceinline__ uint32_t e8m0_pair(uint32_t e2) {
-  // max(E, 8) - 8 on both halves; no borrow crosses halves because each
-  // half is >= 8 after the max.
   return vmax_u16x2(e2, 0x00080008u) - 0x00080008u;
 }
 
-template <int WARPS, int STAGES, int STAGE_BYTES>
-struct MxSmemLayout {
-  static constexpr int kStageBytes = STAGE_BYTES;
-  static constexpr int kDynamicBytes = WARPS * STAGES * STAGE_BYTES + 128;  // + alignment pad
+__device__ __forceinline__ uint32_t half16(uint32_t pair, int which) {
+  return (pair >> (16 * which)) & 0xFFFFu;
+}
+
+// Exponent fields of a packed pair of bf16 magnitudes, as two 16-bit lanes.
+__device__ __forceinline__ uint32_t bf16_exponents(uint32_t m) { return (m >> 7) & 0x00FF00FFu; }
+
+__device__ __forceinline__ void bar_sync_cta(int threads) {
+  asm volatile("bar.sync 1, %0;" :: "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory layout of one CTA
+// ---------------------------------------------------------------------------
+
+template <int WARPS, int OPERANDS>
+struct MxLayout {
+  static constexpr int BAND = 32 * WARPS;
+  static constexpr int TILE_BYTES = BAND * MX_TILE_K * 2;            // one bf16 operand
+  static constexpr int STAGE_BYTES = TILE_BYTES * OPERANDS;
+  static constexpr int STAGES = 2;
+  static constexpr int QCOL_HALF = 128 * MX_TILE_K;                  // 128 m x 128 k codes
+  static constexpr int QCOL_HALVES = BAND / 128;
+  static constexpr int OFF_QCOL = STAGES * STAGE_BYTES;              // 1024-aligned
+  static constexpr int OFF_RSC = OFF_QCOL + QCOL_HALVES * QCOL_HALF; // [BAND][8 slots][4]
+  static constexpr int OFF_CSC = OFF_RSC + BAND * 32;                // [128 cols][8 blocks]
+  static constexpr int OFF_DB = OFF_CSC + MX_TILE_K * 8;             // [WARPS][128] fp32
+  static constexpr int BYTES = OFF_DB + WARPS * MX_TILE_K * 4;
+  static constexpr int DYNAMIC = BYTES + 1024;                       // + alignment pad
 };
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int MODE, bool DBIAS, int ACT, int WARPS, int STAGES>
+template <int MODE, bool DBIAS, int ACT, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1)
-mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const MxArgs a) {
+mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                   const __grid_constant__ CUtensorMap tmap_qcol, const MxArgs a) {
   constexpr bool ROW = (MODE & MX_ROW) != 0;
   constexpr bool COL = (MODE & MX_COL) != 0;
   constexpr int OPERANDS = (ACT == ACT_SWIGLU) ? 2 : 1;
-  constexpr int TILE_BYTES = MX_TILE_M * MX_TILE_K * 2;
-  constexpr int STAGE_BYTES = TILE_BYTES * OPERANDS;
-  constexpr int ROW_PITCH = MX_TILE_K * 2;   // bytes per tile row in shared memory
+  using L = MxLayout<WARPS, OPERANDS>;
+  constexpr int THREADS = WARPS * 32;
+  constexpr int BAND = L::BAND;
+  constexpr int ROW_PITCH = MX_TILE_K * 2;   // bf16 tile row, bytes
   static_assert(!(DBIAS && ACT != ACT_NONE), "dbias is defined on the plain path only");
+  static_assert(BAND % 128 == 0 && BAND <= 256, "colwise codes leave in 128-row halves");
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[WARPS][STAGES];
-  __shared__ __align__(16) uint32_t row_scale_stage[WARPS][32];
+  __shared__ __align__(8) uint64_t full_bar[L::STAGES];
 
-  uint8_t* smem = align_up_shared<128>(smem_raw);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int h = lane >> 4;     // which 16-row half of the tile
+  uint8_t* smem = align_up_shared<1024>(smem_raw);
+  const uint32_t sbase = smem_addr(smem);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int h = lane >> 4;     // which 16-row half of the warp's 32 rows
   const int c = lane & 15;     // which 8-column chunk
-  const uint32_t stage0 = smem_addr(smem) + warp * STAGES * STAGE_BYTES;
-  const uint32_t bar0 = smem_addr(&bars[warp][0]);
-  const uint32_t rs_stage = smem_addr(&row_scale_stage[warp][0]);
+  const uint32_t bar0 = smem_addr(&full_bar[0]);
 
-  const Schedule sched = make_schedule(a, blockIdx.x * WARPS + warp, gridDim.x * WARPS, DBIAS);
-  if (sched.count == 0) return;
+  // This CTA's contiguous range of steps; step t = band * tiles_k + tk.
+  const int64_t total = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
+  const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
+  const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
+  const int count = t1 - t0;
+  if (count <= 0) return;
 
-  if (lane == 0) {
-    prefetch_tensormap(&tmap);
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
-
-  auto issue = [&](int j) {   // lane 0 only
-    int tm, tk;
-    sched.coords(j, tm, tk);
-    const int s = j % STAGES;
-    const uint32_t bar = bar0 + 8 * s;
-    const uint32_t dst = stage0 + s * STAGE_BYTES;
-    mbar_arrive_expect_tx(bar, STAGE_BYTES);
-    tma_load_2d(dst, &tmap, tk * MX_TILE_K, tm * MX_TILE_M, bar);
-    if (OPERANDS == 2) tma_load_2d(dst + TILE_BYTES, &tmap, a.up_col + tk * MX_TILE_K, tm * MX_TILE_M, bar);
+  auto issue_load = [&](int j) {   // thread 0 only
+    const int t = t0 + j;
+    const int band = t / a.tiles_k;
+    const int tk = t - band * a.tiles_k;
+    const int s = j & 1;
+    const uint32_t dst = sbase + s * L::STAGE_BYTES;
+    mbar_arrive_expect_tx(bar0 + 8 * s, L::STAGE_BYTES);
+    tma_load_2d(dst, &tmap_x, tk * MX_TILE_K, band * BAND, bar0 + 8 * s);
+    if (OPERANDS == 2)
+      tma_load_2d(dst + L::TILE_BYTES, &tmap_x, a.up_col + tk * MX_TILE_K, band * BAND,
+                  bar0 + 8 * s);
   };
 
-  if (lane == 0) {
-    const int pre = sched.count < STAGES ? sched.count : STAGES;
-    for (int j = 0; j < pre; ++j) issue(j);
+  if (tid == 0) {
+    prefetch_tensormap(&tmap_x);
+    if (COL) prefetch_tensormap(&tmap_qcol);
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    fence_barrier_init();
+    issue_load(0);
+    if (count > 1) issue_load(1);
   }
+  __syncthreads();
 
-  float dsum[8];
+  const int nmb = a.M / 32;    // colwise scale bytes per column
+  const int nkb = a.K / 32;    // rowwise scale bytes per row
+  int rsc_first = -1;          // first step slot gathered in the rowwise scale staging
+
+  for (int j = 0; j < count; ++j) {
+    const int s = j & 1;
+    const int t = t0 + j;
+    const int band = t / a.tiles_k;
+    const int tk = t - band * a.tiles_k;
+    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (j >> 1) & 1, a.timeout_ns);
+
+    const uint32_t my_row0 =
+        sbase + s * L::STAGE_BYTES + (32 * warp + 16 * h) * ROW_PITCH + c * 16;
+
+    // ---- load this lane's 16 x 8 block and reduce it to magnitude maxima --
+    // y[i][jc]: the values to quantize (fp32).  ce[p] / re[q]: exponent
+    // fields of the largest magnitudes of columns 2p, 2p+1 / rows 2q, 2q+1,
+    // packed as two 16-bit lanes.
+    // The plain path keeps the packed bf16 pairs (xr) and widens them where
+    // they are used; the activation paths hold y in fp32.
+    uint32_t xr[ACT == ACT_NONE ? 16 : 1][4];
+    float y[ACT == ACT_NONE ? 1 : 16][8];
+    uint32_t ce[4] = {0u, 0u, 0u, 0u};
+    uint32_t re[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (ok) {
+      if constexpr (ACT == ACT_NONE) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) dsum[j] = 0.0f;
-  int last_tk = 0;
-
-  for (int j = 0; j < sched.count; ++j) {
-    const int s = j % STAGES;
-    const uint32_t parity = (j / STAGES) & 1;
-    const bool ok = mbar_wait_bounded(bar0 + 8 * s, parity, a.timeout_ns);
-    if (__any_sync(0xFFFFFFFFu, !ok)) {
-      // A copy never landed.  Record it, let this warp's other copies in
-      // flight finish (bounded), and stop without touching more output.
-      if (lane == 0 && a.dev_err) atomicOr(a.dev_err, 1u);
-      const int last = (j + STAGES < sched.count) ? j + STAGES : sched.count;
-      for (int jj = j + 1; jj < last; ++jj)
-        mbar_wait_bounded(bar0 + 8 * (jj % STAGES), (jj / STAGES) & 1, a.timeout_ns);
-      return;
-    }
-
-    int tm, tk;
-    sched.coords(j, tm, tk);
-    last_tk = tk;
-    const uint32_t tile = stage0 + s * STAGE_BYTES;
-    const uint32_t my_row0 = tile + (16 * h) * ROW_PITCH + c * 16;
-
-    // ---- load this lane's 16 x 8 block; reduce to exponent maxima -------
-    // ce[p]: packed exponent maxima of columns 2p (low half), 2p+1 (high).
-    // re[q]: packed exponent maxima of rows 2q (low half), 2q+1 (high).
-    uint32_t ce[4], re[8];
-    uint32_t xr[16][4];
-    float y[(ACT == ACT_NONE) ? 1 : 16][(ACT == ACT_NONE) ? 1 : 8];
-
-    if constexpr (ACT == ACT_NONE) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint4 v = lds128(my_row0 + i * ROW_PITCH);
-        xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
-      }
-      uint32_t cm[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        uint32_t t[2];
-#pragma unroll
-        for (int di = 0; di < 2; ++di) {
-          const uint32_t a0 = xr[i + di][0] & 0x7FFF7FFFu;
-          const uint32_t a1 = xr[i + di][1] & 0x7FFF7FFFu;
-          const uint32_t a2 = xr[i + di][2] & 0x7FFF7FFFu;
-          const uint32_t a3 = xr[i + di][3] & 0x7FFF7FFFu;
-          cm[0] = vmax_u16x2(cm[0], a0);
-          cm[1] = vmax_u16x2(cm[1], a1);
-          cm[2] = vmax_u16x2(cm[2], a2);
-          cm[3] = vmax_u16x2(cm[3], a3);
-          t[di] = vmax_u16x2(vmax_u16x2(a0, a1), vmax_u16x2(a2, a3));
+        for (int i = 0; i < 16; ++i) {
+          const uint4 v = lds128(my_row0 + i * ROW_PITCH);
+          xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
         }
-        // low halves = even columns, high = odd; fold to one max per row.
-        const uint32_t rm = vmax_u16x2(prmt(t[0], t[1], 0x5410), prmt(t[0], t[1], 0x7632));
-        re[i / 2] = (rm >> 7) & 0x00FF00FFu;      // bf16 magnitude -> exponent field
-      }
+        uint32_t cm[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-      for (int p = 0; p < 4; ++p) ce[p] = (cm[p] >> 7) & 0x00FF00FFu;
-    } else {
+        for (int i = 0; i < 16; i += 2) {
+          uint32_t tt[2];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint4 v = lds128(my_row0 + i * ROW_PITCH);
-        uint32_t u[4] = {0u, 0u, 0u, 0u};
-        if constexpr (ACT == ACT_SWIGLU) {
-          const uint4 w = lds128(my_row0 + TILE_BYTES + i * ROW_PITCH);
-          u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w;
+          for (int di = 0; di < 2; ++di) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], xr[i + di][p]);
+            tt[di] = absmax_bf16x2(absmax_bf16x2(xr[i + di][0], xr[i + di][1]),
+                                   absmax_bf16x2(xr[i + di][2], xr[i + di][3]));
+          }
+          // low halves: even columns, high halves: odd columns; fold per row.
+          re[i / 2] = bf16_exponents(
+              absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)));
         }
-        const uint32_t g[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          if constexpr (ACT == ACT_GELU) {
-            y[i][2 * p] = gelu_tanh_f32(bf16_lo(g[p]));
-            y[i][2 * p + 1] = gelu_tanh_f32(bf16_hi(g[p]));
-          } else {
-            y[i][2 * p] = swiglu_f32(bf16_lo(g[p]), bf16_lo(u[p]));
-            y[i][2 * p + 1] = swiglu_f32(bf16_hi(g[p]), bf16_hi(u[p]));
+        for (int p = 0; p < 4; ++p) ce[p] = bf16_exponents(cm[p]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 v = lds128(my_row0 + i * ROW_PITCH);
+          uint32_t u[4] = {0u, 0u, 0u, 0u};
+          if constexpr (ACT == ACT_SWIGLU) {
+            const uint4 w = lds128(my_row0 + L::TILE_BYTES + i * ROW_PITCH);
+            u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w;
+          }
+          const uint32_t g[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            if constexpr (ACT == ACT_GELU) {
+              y[i][2 * p] = gelu_tanh_f32(bf16_lo(g[p]));
+              y[i][2 * p + 1] = gelu_tanh_f32(bf16_hi(g[p]));
+            } else {
+              y[i][2 * p] = swiglu_f32(bf16_lo(g[p]), bf16_lo(u[p]));
+              y[i][2 * p + 1] = swiglu_f32(bf16_hi(g[p]), bf16_hi(u[p]));
+            }
           }
         }
-      }
-      uint32_t cmx[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-      uint32_t rmx[16];
+        uint32_t cmx[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint32_t rmx[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        rmx[i] = 0u;
+        for (int i = 0; i < 16; ++i) {
+          rmx[i] = 0u;
 #pragma unroll
-        for (int jc = 0; jc < 8; ++jc) {
-          const uint32_t b = __float_as_uint(y[i][jc]) & 0x7FFFFFFFu;
-          cmx[jc] = max(cmx[jc], b);
-          rmx[i] = max(rmx[i], b);
+          for (int jc = 0; jc < 8; ++jc) {
+            const uint32_t b = __float_as_uint(y[i][jc]) & 0x7FFFFFFFu;
+            cmx[jc] = max(cmx[jc], b);
+            rmx[i] = max(rmx[i], b);
+          }
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) re[q] = (rmx[2 * q] >> 23) | ((rmx[2 * q + 1] >> 23) << 16);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) ce[p] = (cmx[2 * p] >> 23) | ((cmx[2 * p + 1] >> 23) << 16);
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) re[q] = (rmx[2 * q] >> 23) | ((rmx[2 * q + 1] >> 23) << 16);
-#pragma unroll
-      for (int p = 0; p < 4; ++p) ce[p] = (cmx[2 * p] >> 23) | ((cmx[2 * p + 1] >> 23) << 16);
     }
 
-    // ---- every value of the slot is in registers: hand it back to TMA ----
+    // ---- barrier A: the slot has been read by every warp, the colwise
+    // staging is free (thread 0 waited for the previous store), and every
+    // thread knows whether the copy landed. -------------------------------
     fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && j + STAGES < sched.count) issue(j + STAGES);
+    if (COL && tid == 0) bulk_wait_read<0>();
+    if (__syncthreads_or(!ok)) {
+      // A copy never landed: record it, let the other copy in flight and the
+      // pending stores finish (bounded), and stop without more output.
+      if (tid == 0) {
+        if (a.dev_err) atomicOr(a.dev_err, 1u);
+        if (j + 1 < count)
+          mbar_wait_bounded(bar0 + 8 * (s ^ 1), ((j + 1) >> 1) & 1, a.timeout_ns);
+        bulk_wait_all();
+      }
+      return;
+    }
+    if (tid == 0 && j + 2 < count) issue_load(j + 2);
 
     // ---- complete the block maxima across lanes -------------------------
 #pragma unroll
@@ -297,19 +295,22 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const MxArgs a) {
 #pragma unroll
     for (int p = 0; p < 4; ++p) ce[p] = vmax_u16x2(ce[p], __shfl_xor_sync(0xFFFFFFFFu, ce[p], 16));
 
-    const int col0 = tk * MX_TILE_K + c * 8;      // first column of this lane
+    const int col0 = tk * MX_TILE_K + c * 8;            // first column of this lane
     const bool col_ok = col0 < a.K;
-    const int row0 = tm * MX_TILE_M + 16 * h;     // first row of this lane
+    const int row0 = band * BAND + 32 * warp + 16 * h;  // first row of this lane
+    const bool row_ok = row0 < a.M;
+    const int slot = tk & 7;                            // rowwise scale gathering slot
 
-    auto val = [&](int i, int jc) -> float {
+    // Values of row i, columns 2p and 2p+1 as an fp32 pair.
+    auto pair_at = [&](int i, int p) -> float2 {
       if constexpr (ACT == ACT_NONE) {
-        return (jc & 1) ? bf16_hi(xr[i][jc >> 1]) : bf16_lo(xr[i][jc >> 1]);
+        return make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p]));
       } else {
-        return y[i][jc];
+        return make_float2(y[i][2 * p], y[i][2 * p + 1]);
       }
     };
 
-    // ---- rowwise: scale codes, codes, stores ----------------------------
+    // ---- rowwise: codes straight to global, scale bytes to staging --------
     if constexpr (ROW) {
       uint32_t rc[8];
 #pragma unroll
@@ -317,101 +318,172 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const MxArgs a) {
       uint8_t* qrow = a.q_row + static_cast<size_t>(row0) * a.K + col0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const uint32_t code = (rc[i >> 1] >> (16 * (i & 1))) & 0xFFu;
-        const float inv = inv_scale_from_e8m0(code);
-        const uint32_t w0 = cvt_e4m3x4(val(i, 0) * inv, val(i, 1) * inv, val(i, 2) * inv, val(i, 3) * inv);
-        const uint32_t w1 = cvt_e4m3x4(val(i, 4) * inv, val(i, 5) * inv, val(i, 6) * inv, val(i, 7) * inv);
-        if (col_ok) stg64(qrow + static_cast<size_t>(i) * a.K, w0, w1);
-      }
-      // Scale bytes: lane (h, c) holds the codes of block c/4 for its 16
-      // rows; it stages rows 4t + (c & 3) into a [32 rows][4 blocks] byte
-      // array, then lane L writes row L's 4 bytes.
-      const int r = c & 3, b = c >> 2;
+        const float inv = inv_scale_from_e8m0(half16(rc[i >> 1], i & 1));
+        const float2 iv = make_float2(inv, inv);
+        uint32_t w[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint32_t pair = (r >> 1) ? rc[2 * t + 1] : rc[2 * t];
-        sts8(rs_stage + (16 * h + 4 * t + r) * 4 + b, (pair >> (16 * (r & 1))) & 0xFFu);
+        for (int p = 0; p < 4; ++p) {
+          const float2 v = mul_f32x2(pair_at(i, p), iv);
+          w[p] = cvt_e4m3x2(v.x, v.y);
+        }
+        if (col_ok && row_ok)
+          stg64(qrow + static_cast<size_t>(i) * a.K, w[0] | (w[1] << 16), w[2] | (w[3] << 16));
       }
-      __syncwarp();
-      const uint32_t w = lds32(rs_stage + lane * 4);
-      const int kb0 = tk * (MX_TILE_K / 32);
-      const int nkb = a.K / 32;
-      const int valid = min(4, nkb - kb0);
-      uint8_t* srow = a.s_row + static_cast<size_t>(tm * MX_TILE_M + lane) * nkb + kb0;
-      if (valid == 4 && (nkb & 3) == 0) {
-        stg32(srow, w);
-      } else {
-        for (int bb = 0; bb < valid; ++bb) stg8(srow + bb, (w >> (8 * bb)) & 0xFFu);
+      // Lane (h, c) holds block c/4's codes for its 16 rows; it stages rows
+      // 4t + (c & 3) into [BAND rows][8 slots][4 blocks].
+      const int r = c & 3, b = c >> 2;
+      const uint32_t rs = sbase + L::OFF_RSC + (32 * warp + 16 * h) * 32 + slot * 4 + b;
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) {
+        const uint32_t pair = (r >> 1) ? rc[2 * t4 + 1] : rc[2 * t4];
+        sts8(rs + (4 * t4 + r) * 32, (pair >> (16 * (r & 1))) & 0xFFu);
       }
     }
 
-    // ---- colwise: scale codes, codes, stores ----------------------------
+    // ---- colwise: codes and scale bytes to staging -------------------------
     if constexpr (COL) {
       uint32_t cc[4];
 #pragma unroll
       for (int p = 0; p < 4; ++p) cc[p] = e8m0_pair(ce[p]);
-      uint8_t* qcol = a.q_col + static_cast<size_t>(col0) * a.M + row0;
+      // Staging half (warp / 4) holds m = 128 * half + 0..127 as
+      // [k % 8][k / 8][128 m], the 16-byte chunk index xor-ed with (k / 8) % 8
+      // (the 128-byte swizzle of the store's tensor map).
+      const uint32_t qs = sbase + L::OFF_QCOL + (warp >> 2) * L::QCOL_HALF + c * 128 +
+                          ((((warp & 3) * 2 + h) ^ (c & 7)) << 4);
 #pragma unroll
-      for (int jc = 0; jc < 8; ++jc) {
-        const uint32_t code = (cc[jc >> 1] >> (16 * (jc & 1))) & 0xFFu;
-        const float inv = inv_scale_from_e8m0(code);
-        uint32_t w[4];
+      for (int p = 0; p < 4; ++p) {
+        const float2 iv = make_float2(inv_scale_from_e8m0(half16(cc[p], 0)),
+                                      inv_scale_from_e8m0(half16(cc[p], 1)));
+        uint32_t we[8], wo[8];   // codes of columns 2p (even) and 2p+1 (odd), two rows each
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          w[q] = cvt_e4m3x4(val(4 * q, jc) * inv, val(4 * q + 1, jc) * inv,
-                            val(4 * q + 2, jc) * inv, val(4 * q + 3, jc) * inv);
-        if (col_ok) stg128(qcol + static_cast<size_t>(jc) * a.M, w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 16; i += 2) {
+          const float2 r0 = mul_f32x2(pair_at(i, p), iv);
+          const float2 r1 = mul_f32x2(pair_at(i + 1, p), iv);
+          we[i / 2] = cvt_e4m3x2(r0.x, r1.x);
+          wo[i / 2] = cvt_e4m3x2(r0.y, r1.y);
+        }
+        sts128(qs + (2 * p) * 2048, we[0] | (we[1] << 16), we[2] | (we[3] << 16),
+               we[4] | (we[5] << 16), we[6] | (we[7] << 16));
+        sts128(qs + (2 * p + 1) * 2048, wo[0] | (wo[1] << 16), wo[2] | (wo[3] << 16),
+               wo[4] | (wo[5] << 16), wo[6] | (wo[7] << 16));
       }
-      // Lane h = 0 writes the scale bytes of columns 0-3, h = 1 of 4-7.
-      const int nmb = a.M / 32;
+      // Scale bytes: [128 columns][8 row blocks]; h = 0 writes columns 0-3,
+      // h = 1 columns 4-7 of the lane's chunk.
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
-        const uint32_t code = (pair >> (16 * (jj & 1))) & 0xFFu;
-        if (col_ok)
-          stg8(a.s_col + static_cast<size_t>(col0 + 4 * h + jj) * nmb + tm, code);
+        sts8(sbase + L::OFF_CSC + (c * 8 + 4 * h + jj) * 8 + warp,
+             (pair >> (16 * (jj & 1))) & 0xFFu);
       }
     }
 
-    // ---- dbias: column sums of this tile, pairwise over rows -------------
+    // ---- dbias: column sums of the warp's 32 rows, pairwise ----------------
     if constexpr (DBIAS) {
 #pragma unroll
       for (int jc = 0; jc < 8; ++jc) {
         float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = val(i, jc);
+        for (int i = 0; i < 16; ++i) {
+          const float2 pr = pair_at(i, jc >> 1);
+          v[i] = (jc & 1) ? pr.y : pr.x;
+        }
 #pragma unroll
         for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
-        const float tile_sum = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
-        dsum[jc] += tile_sum;
+        const float s32 = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
+        if (h == 0) {
+          float* db = reinterpret_cast<float*>(smem + L::OFF_DB) + warp * MX_TILE_K + c * 8 + jc;
+          *db = s32;
+        }
       }
     }
-    __syncwarp();   // row_scale_stage is rewritten by the next tile
-  }
 
-  if constexpr (DBIAS) {
-    // This warp's column strip is fixed; write its partial sums once.
-    const int col0 = last_tk * MX_TILE_K + c * 8;
-    if (h == 0 && col0 < a.K) {
-      const int p = sched.first;
-      float* dst = a.dbias_ws + static_cast<size_t>(p) * a.K + col0;
-      stg128(dst, __float_as_uint(dsum[0]), __float_as_uint(dsum[1]),
-             __float_as_uint(dsum[2]), __float_as_uint(dsum[3]));
-      stg128(dst + 4, __float_as_uint(dsum[4]), __float_as_uint(dsum[5]),
-             __float_as_uint(dsum[6]), __float_as_uint(dsum[7]));
+    // ---- barrier B: the band's staging is complete -------------------------
+    fence_proxy_async_smem();
+    bar_sync_cta(THREADS);
+
+    if constexpr (COL) {
+      if (tid == 0) {
+#pragma unroll
+        for (int half = 0; half < L::QCOL_HALVES; ++half)
+          tma_store_3d(&tmap_qcol, sbase + L::OFF_QCOL + half * L::QCOL_HALF,
+                       band * BAND + 128 * half, tk * (MX_TILE_K / 8), 0);
+        bulk_commit();
+      }
+      // Colwise scale bytes: one run of the band's blocks per column.
+      if (tid < MX_TILE_K) {
+        const int k = tk * MX_TILE_K + tid;
+        const int mb0 = band * (BAND / 32);
+        const int nvalid = min(BAND / 32, nmb - mb0);
+        if (k < a.K) {
+          uint8_t* dst = a.s_col + static_cast<size_t>(k) * nmb + mb0;
+          const uint32_t src = sbase + L::OFF_CSC + tid * 8;
+          const uint32_t lo = lds32(src), hi = lds32(src + 4);
+          if (BAND == 256 && nvalid == 8 && (nmb & 7) == 0) {
+            stg64(dst, lo, hi);
+          } else if (BAND == 128 && nvalid == 4 && (nmb & 3) == 0) {
+            stg32(dst, lo);
+          } else {
+            for (int bb = 0; bb < nvalid; ++bb)
+              stg8(dst + bb, ((bb < 4 ? lo : hi) >> (8 * (bb & 3))) & 0xFFu);
+          }
+        }
+      }
+    }
+
+    if constexpr (ROW) {
+      if (rsc_first < 0) rsc_first = slot;
+      const bool flush = (slot == 7) || (tk + 1 == a.tiles_k) || (j + 1 == count);
+      if (flush) {
+        // Rowwise scale bytes of steps rsc_first..slot of this group of eight:
+        // one 32-byte sector per row when all eight steps are present.
+        const int row = band * BAND + tid;
+        if (row < a.M) {
+          const int kb0 = (tk - slot) * 4;   // first k-block of the group
+          uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
+          const uint32_t src = sbase + L::OFF_RSC + tid * 32;
+          if (rsc_first == 0 && slot == 7 && (nkb & 7) == 0) {
+            const uint4 lo = lds128(src), hi = lds128(src + 16);
+            stg128(dst, lo.x, lo.y, lo.z, lo.w);
+            stg128(dst + 16, hi.x, hi.y, hi.z, hi.w);
+          } else {
+            const int b_end = min((slot + 1) * 4, nkb - kb0);
+            for (int bb = rsc_first * 4; bb < b_end; ++bb)
+              stg8(dst + bb, (lds32(src + (bb & ~3)) >> (8 * (bb & 3))) & 0xFFu);
+          }
+        }
+        rsc_first = -1;
+      }
+    }
+
+    if constexpr (DBIAS) {
+      // The band's sum of each column: pairwise over the warps' 32-row sums.
+      if (tid < MX_TILE_K) {
+        const int k = tk * MX_TILE_K + tid;
+        const float* db = reinterpret_cast<const float*>(smem + L::OFF_DB) + tid;
+        float v[WARPS];
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) v[w] = db[w * MX_TILE_K];
+#pragma unroll
+        for (int w = WARPS / 2; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
+        if (k < a.K) a.dbias_ws[static_cast<size_t>(band) * a.K + k] = v[0];
+      }
     }
   }
+  // The staged codes must have left shared memory before the CTA exits.
+  if (tid == 0) bulk_wait_all();
 }
 
-// dbias[k] = sum over row groups of the partial sums, in group order.
-__global__ void dbias_finalize_kernel(const float* __restrict__ ws, int groups, int K,
+// dbias[k] = sum over bands of the band sums, in band order.
+__global__ void dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K,
                                       float* __restrict__ dbias) {
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= K) return;
   float s = 0.0f;
-  for (int p = 0; p < groups; ++p) s += ws[static_cast<size_t>(p) * K + k];
+  for (int p = 0; p < bands; ++p) s += ws[static_cast<size_t>(p) * K + k];
   dbias[k] = s;
 }
 
@@ -419,87 +491,69 @@ __global__ void dbias_finalize_kernel(const float* __restrict__ ws, int groups, 
 // Launch configuration per variant
 // ---------------------------------------------------------------------------
 
+// Warps per CTA (= 32-row slices of a band); one CTA per SM.
 template <int ACT>
 struct MxConfig {
-  // 8 warps x 3 slots x 8 KiB = 192 KiB of tiles per SM.
-  static constexpr int WARPS = 8;
-  static constexpr int STAGES = 3;
+  static constexpr int WARPS = 8;   // band of 256 rows, 64 KiB per slot
 };
 template <>
 struct MxConfig<ACT_SWIGLU> {
-  // gate + up per slot: 6 warps x 2 slots x 16 KiB = 192 KiB per SM.
-  static constexpr int WARPS = 6;
-  static constexpr int STAGES = 2;
+  static constexpr int WARPS = 4;   // band of 128 rows, gate + up = 64 KiB per slot
 };
 
 template <int MODE, bool DBIAS, int ACT>
-cudaError_t launch_variant(const CUtensorMap& map, const MxArgs& a, int num_sms,
+cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
                            cudaStream_t stream) {
   constexpr int WARPS = MxConfig<ACT>::WARPS;
-  constexpr int STAGES = MxConfig<ACT>::STAGES;
-  constexpr int STAGE_BYTES = MX_TILE_M * MX_TILE_K * 2 * (ACT == ACT_SWIGLU ? 2 : 1);
-  constexpr int SMEM = WARPS * STAGES * STAGE_BYTES + 128;
-  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS, STAGES>;
+  using L = MxLayout<WARPS, ACT == ACT_SWIGLU ? 2 : 1>;
+  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS>;
 
   static int configured_device = -1;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (configured_device != dev) {
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYNAMIC);
     if (err != cudaSuccess) return err;
     configured_device = dev;
   }
-
-  int grid;
-  if (DBIAS) {
-    const int warps_needed = a.dbias_groups * a.tiles_k;
-    grid = (warps_needed + WARPS - 1) / WARPS;
-  } else {
-    const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
-    const int64_t ctas_for_tiles = (tiles + WARPS - 1) / WARPS;
-    grid = static_cast<int>(ctas_for_tiles < num_sms ? ctas_for_tiles : num_sms);
-  }
-  if (grid < 1) grid = 1;
-  kernel<<<grid, WARPS * 32, SMEM, stream>>>(map, a);
+  const int64_t steps = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
+  const int grid = static_cast<int>(steps < num_sms ? steps : num_sms);
+  kernel<<<grid < 1 ? 1 : grid, WARPS * 32, L::DYNAMIC, stream>>>(maps.x, maps.q_col, a);
   return cudaGetLastError();
 }
 
 template <bool DBIAS, int ACT>
-cudaError_t launch_mode(const CUtensorMap& map, const MxArgs& a, int mode, int num_sms,
+cudaError_t launch_mode(const MxMaps& maps, const MxArgs& a, int mode, int num_sms,
                         cudaStream_t stream) {
   switch (mode) {
-    case MX_ROW: return launch_variant<MX_ROW, DBIAS, ACT>(map, a, num_sms, stream);
-    case MX_COL: return launch_variant<MX_COL, DBIAS, ACT>(map, a, num_sms, stream);
-    default: return launch_variant<MX_ROW | MX_COL, DBIAS, ACT>(map, a, num_sms, stream);
+    case MX_ROW: return launch_variant<MX_ROW, DBIAS, ACT>(maps, a, num_sms, stream);
+    case MX_COL: return launch_variant<MX_COL, DBIAS, ACT>(maps, a, num_sms, stream);
+    default: return launch_variant<MX_ROW | MX_COL, DBIAS, ACT>(maps, a, num_sms, stream);
   }
 }
 
 }  // namespace
 
-int mx_dbias_groups(int tiles_m, int tiles_k, int num_sms) {
-  const int warp_capacity = num_sms * MxConfig<ACT_NONE>::WARPS;
-  int groups = warp_capacity / tiles_k;
-  if (groups < 1) groups = 1;
-  if (groups > tiles_m) groups = tiles_m;
-  return groups;
+int mx_band_rows(int act) {
+  return 32 * (act == ACT_SWIGLU ? MxConfig<ACT_SWIGLU>::WARPS : MxConfig<ACT_NONE>::WARPS);
 }
 
-cudaError_t launch_mx(const CUtensorMap& map, const MxArgs& a, int mode, bool dbias, int act,
+cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
                       int num_sms, cudaStream_t stream) {
-  if (dbias) return launch_mode<true, ACT_NONE>(map, a, mode, num_sms, stream);
+  if (dbias) return launch_mode<true, ACT_NONE>(maps, a, mode, num_sms, stream);
   switch (act) {
-    case ACT_GELU: return launch_mode<false, ACT_GELU>(map, a, mode, num_sms, stream);
-    case ACT_SWIGLU: return launch_mode<false, ACT_SWIGLU>(map, a, mode, num_sms, stream);
-    default: return launch_mode<false, ACT_NONE>(map, a, mode, num_sms, stream);
+    case ACT_GELU: return launch_mode<false, ACT_GELU>(maps, a, mode, num_sms, stream);
+    case ACT_SWIGLU: return launch_mode<false, ACT_SWIGLU>(maps, a, mode, num_sms, stream);
+    default: return launch_mode<false, ACT_NONE>(maps, a, mode, num_sms, stream);
   }
 }
 
-cudaError_t launch_dbias_finalize(const float* ws, int groups, int K, float* dbias,
+cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
                                   cudaStream_t stream) {
   const int threads = 256;
   const int blocks = (K + threads - 1) / threads;
-  dbias_finalize_kernel<<<blocks, threads, 0, stream>>>(ws, groups, K, dbias);
+  dbias_finalize_kernel<<<blocks, threads, 0, stream>>>(ws, bands, K, dbias);
   return cudaGetLastError();
 }
 

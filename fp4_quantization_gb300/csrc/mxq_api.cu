@@ -49,10 +49,7 @@ mxq_status current_device(int* num_sms) {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-// Encodes a 2-D bf16 tensor map over x[rows][cols] (row stride ldx
-// elements) with a box of box_cols x box_rows; out-of-range reads give 0.
-mxq_status encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols,
-                           int64_t ldx, int box_cols, int box_rows) {
+bool load_encoder() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -61,16 +58,42 @@ mxq_status encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
-  if (!g_encode) return MXQ_ECUDA;
+  return g_encode != nullptr;
+}
+
+// Encodes a tensor map of `rank` dimensions (innermost first) with no
+// swizzle; out-of-range loads read 0 and out-of-range stores are dropped.
+mxq_status encode_map(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base,
+                      const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                      const cuuint32_t* box,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
+  if (!load_encoder()) return MXQ_ECUDA;
+  const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(map, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                              dims, strides_bytes, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MXQ_OK : MXQ_ECUDA;
+}
+
+// 2-D bf16 map over x[rows][cols] (row stride ldx elements).
+mxq_status encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols,
+                           int64_t ldx, int box_cols, int box_rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims,
-                              strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MXQ_OK : MXQ_ECUDA;
+  return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box);
+}
+
+// Colwise-code map of an MXFP8 call quantizing an M x K matrix: [K][M]
+// seen as [k % 8][k / 8][m], box 128 m x 16 x 8, 128-byte swizzle.
+mxq_status encode_mx_qcol_map(CUtensorMap* map, int64_t M, int64_t K, uint8_t* q_col) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 8), 8};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(8 * M), static_cast<cuuint64_t>(M)};
+  const cuuint32_t box[3] = {128, mxq::MX_TILE_K / 8, 8};
+  return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q_col, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -113,12 +136,9 @@ size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags) {
   if (M <= 0 || K <= 0) return 0;
   if (op == MXQ_OP_NVFP4) return 16;   // one fp32 amax, padded
   if (op != MXQ_OP_ROWCOL || !(flags & MXQ_DBIAS)) return 0;
-  int sms = 0;
-  if (current_device(&sms) != MXQ_OK) return 0;
-  const int tiles_m = static_cast<int>(M / mxq::MX_TILE_M);
-  const int tiles_k = static_cast<int>((K + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
-  const int groups = mxq::mx_dbias_groups(tiles_m, tiles_k, sms);
-  return static_cast<size_t>(groups) * static_cast<size_t>(K) * sizeof(float);
+  const int64_t band = mxq::mx_band_rows(mxq::ACT_NONE);
+  const int64_t bands = (M + band - 1) / band;
+  return static_cast<size_t>(bands) * static_cast<size_t>(K) * sizeof(float);
 }
 
 mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t flags,
@@ -149,10 +169,12 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   st = check_mx_outputs(flags, K, q_row, s_row, q_col, s_col);
   if (st != MXQ_OK) return st;
 
+  const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_GELU : mxq::ACT_NONE;
+  const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
-  a.tiles_m = static_cast<int>(M / mxq::MX_TILE_M);
+  a.tiles_m = static_cast<int>((M + band - 1) / band);
   a.tiles_k = static_cast<int>((K + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
   a.q_row = q_row;
   a.s_row = s_row;
@@ -161,19 +183,21 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   if (want_dbias) {
-    a.dbias_groups = mxq::mx_dbias_groups(a.tiles_m, a.tiles_k, sms);
-    const size_t need = static_cast<size_t>(a.dbias_groups) * static_cast<size_t>(K) * sizeof(float);
+    const size_t need = static_cast<size_t>(a.tiles_m) * static_cast<size_t>(K) * sizeof(float);
     if (!workspace || workspace_bytes < need) return MXQ_EWORKSPACE;
     if (!aligned(workspace, 16)) return MXQ_EALIGN;
     a.dbias_ws = static_cast<float*>(workspace);
   }
-  CUtensorMap map;
-  st = encode_bf16_map(&map, x, M, K, ldx, mxq::MX_TILE_K, mxq::MX_TILE_M);
+  mxq::MxMaps maps{};
+  st = encode_bf16_map(&maps.x, x, M, K, ldx, mxq::MX_TILE_K, band);
   if (st != MXQ_OK) return st;
-  const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_GELU : mxq::ACT_NONE;
-  st = from_cuda(mxq::launch_mx(map, a, direction_mode(flags), want_dbias, act, sms, stream));
+  if (flags & MXQ_COLWISE) {
+    st = encode_mx_qcol_map(&maps.q_col, M, K, q_col);
+    if (st != MXQ_OK) return st;
+  }
+  st = from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
   if (st != MXQ_OK || !want_dbias) return st;
-  return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.dbias_groups, a.K, dbias, stream));
+  return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
 }
 
 mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, uint32_t flags,
@@ -194,10 +218,11 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
   st = check_mx_outputs(flags, N, q_row, s_row, q_col, s_col);
   if (st != MXQ_OK) return st;
 
+  const int band = mxq::mx_band_rows(mxq::ACT_SWIGLU);
   mxq::MxArgs a{};
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(N);
-  a.tiles_m = static_cast<int>(M / mxq::MX_TILE_M);
+  a.tiles_m = static_cast<int>((M + band - 1) / band);
   a.tiles_k = static_cast<int>((N + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
   a.up_col = static_cast<int>(N);
   a.q_row = q_row;
@@ -206,11 +231,16 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
   a.s_col = s_col;
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
-  CUtensorMap map;
-  // The map spans [gate | up]; gate boxes start at column k, up boxes at N + k.
-  st = encode_bf16_map(&map, x, M, 2 * N, ldx, mxq::MX_TILE_K, mxq::MX_TILE_M);
+  mxq::MxMaps maps{};
+  // The input map spans [gate | up]; gate boxes start at column k, up boxes
+  // at N + k.
+  st = encode_bf16_map(&maps.x, x, M, 2 * N, ldx, mxq::MX_TILE_K, band);
   if (st != MXQ_OK) return st;
-  return from_cuda(mxq::launch_mx(map, a, direction_mode(flags), false, mxq::ACT_SWIGLU, sms, stream));
+  if (flags & MXQ_COLWISE) {
+    st = encode_mx_qcol_map(&maps.q_col, M, N, q_col);
+    if (st != MXQ_OK) return st;
+  }
+  return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, mxq::ACT_SWIGLU, sms, stream));
 }
 
 mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* amax_out,

@@ -8,8 +8,9 @@
 
 namespace mxq {
 
-// MXFP8 warp tile: 32 rows (one colwise block) x 128 columns (four rowwise
-// blocks) of bf16 = 8 KiB, loaded by one TMA box.
+// MXFP8: each warp quantizes 32 rows (one colwise block) x 128 columns
+// (four rowwise blocks); a CTA takes a band of mx_band_rows() rows x 128
+// columns per step.
 constexpr int MX_TILE_M = 32;
 constexpr int MX_TILE_K = 128;
 
@@ -25,16 +26,23 @@ enum : int { ACT_NONE = 0, ACT_GELU = 1, ACT_SWIGLU = 2 };
 
 struct MxArgs {
   int M, K;                 // shape of y (the quantized matrix)
-  int tiles_m, tiles_k;     // MX_TILE_M x MX_TILE_K tiles covering y
+  int tiles_m, tiles_k;     // bands of mx_band_rows() rows, 128-column steps
   int up_col;               // SwiGLU: column of the up half in x; else 0
-  int dbias_groups;         // row groups of the dbias schedule, 0 without dbias
   uint8_t* q_row;
   uint8_t* s_row;
   uint8_t* q_col;
   uint8_t* s_col;
-  float* dbias_ws;          // [dbias_groups][K] partial column sums
+  float* dbias_ws;          // [tiles_m][K] column sums of each band
   uint32_t* dev_err;
   uint64_t timeout_ns;
+};
+
+// TMA descriptors of one MXFP8 call: the bf16 input (box 128 columns x one
+// band) and the colwise codes [K][M] viewed as the 3-D tensor
+// [k % 8][k / 8][m] (box 128 x 16 x 8, 128-byte swizzle).
+struct MxMaps {
+  CUtensorMap x;
+  CUtensorMap q_col;
 };
 
 struct NvArgs {
@@ -50,13 +58,12 @@ struct NvArgs {
   uint64_t timeout_ns;
 };
 
-// Number of row groups the dbias schedule uses on a device with `num_sms`
-// SMs (each group's partial sums take K floats of workspace).
-int mx_dbias_groups(int tiles_m, int tiles_k, int num_sms);
+// Rows per band (per CTA step) of the MXFP8 kernel for activation `act`.
+int mx_band_rows(int act);
 
-cudaError_t launch_mx(const CUtensorMap& map, const MxArgs& a, int mode, bool dbias, int act,
+cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
                       int num_sms, cudaStream_t stream);
-cudaError_t launch_dbias_finalize(const float* ws, int groups, int K, float* dbias,
+cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
                                   cudaStream_t stream);
 cudaError_t launch_nvfp4(const CUtensorMap& map, const NvArgs& a, int mode, int num_sms,
                          cudaStream_t stream);
