@@ -11,16 +11,19 @@
 // the number of L2 write requests rather than by bytes: a 1-byte store costs
 // as much as a 32-byte one.  The kernel is laid out so every output leaves
 // in whole sectors or lines:
-//  * One CTA (WARPS warps, one CTA per SM) walks a contiguous range of
+//  * One CTA (BAND / 16 warps, one CTA per SM) walks a contiguous range of
 //    "steps"; a step is a band of BAND rows x 128 columns, loaded by one
 //    TMA box into a 2-slot ring (one mbarrier per slot).  Steps run along K
 //    inside a band, bands one after another.
-//  * Warp w owns rows 32w..32w+31 of the band; lane (h, c) = (lane / 16,
-//    lane % 16) owns rows 16h..16h+15 and columns 8c..8c+7 of those: 16
+//  * Warp w owns rows 16w..16w+15 of the band; lane (h, c) = (lane / 16,
+//    lane % 16) owns rows 8h..8h+7 and columns 8c..8c+7 of those: 8
 //    conflict-free 16-byte shared loads (a quarter warp reads one contiguous
-//    128-byte row segment).  Colwise 32x1 amax: in-thread over 16 rows + one
-//    xor-16 shuffle; rowwise 1x32 amax: in-thread over 8 columns + xor-1 /
-//    xor-2 shuffles, two rows per register.
+//    128-byte row segment).  Colwise 32x1 amax: in-thread over 8 rows, one
+//    xor-16 shuffle, then the two warps of a 32-row block swap their halves
+//    through shared memory at the step's first barrier; rowwise 1x32 amax:
+//    in-thread over 8 columns + xor-1 / xor-2 shuffles, two rows per
+//    register.  Small per-lane blocks keep registers at or below 128, so
+//    sixteen warps share an SM.
 //  * The shared scale is read off the exponent field of the amax; elements
 //    are multiplied by the exact power of two 2^-e (two per mul.rn.f32x2, no
 //    division; torchao PR #12, rationale) and converted two at a time by
@@ -103,19 +106,20 @@ __device__ __forceinline__ void bar_sync_cta(int threads) {
 // Shared-memory layout of one CTA
 // ---------------------------------------------------------------------------
 
-template <int WARPS, int OPERANDS>
+template <int WARPS, int OPERANDS, int NSTAGES>
 struct MxLayout {
-  static constexpr int BAND = 32 * WARPS;
+  static constexpr int BAND = 16 * WARPS;
   static constexpr int TILE_BYTES = BAND * MX_TILE_K * 2;            // one bf16 operand
   static constexpr int STAGE_BYTES = TILE_BYTES * OPERANDS;
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = NSTAGES;
   static constexpr int QCOL_HALF = 128 * MX_TILE_K;                  // 128 m x 128 k codes
   static constexpr int QCOL_HALVES = BAND / 128;
   static constexpr int OFF_QCOL = STAGES * STAGE_BYTES;              // 1024-aligned
   static constexpr int OFF_RSC = OFF_QCOL + QCOL_HALVES * QCOL_HALF; // [BAND][8 slots][4]
   static constexpr int OFF_CSC = OFF_RSC + BAND * 32;                // [128 cols][8 blocks]
   static constexpr int OFF_DB = OFF_CSC + MX_TILE_K * 8;             // [WARPS][128] fp32
-  static constexpr int BYTES = OFF_DB + WARPS * MX_TILE_K * 4;
+  static constexpr int OFF_XCH = OFF_DB + WARPS * MX_TILE_K * 4;     // [WARPS][16][4] u32
+  static constexpr int BYTES = OFF_XCH + WARPS * 16 * 16;
   static constexpr int DYNAMIC = BYTES + 1024;                       // + alignment pad
 };
 
@@ -123,14 +127,14 @@ struct MxLayout {
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int MODE, bool DBIAS, int ACT, int WARPS>
+template <int MODE, bool DBIAS, int ACT, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_qcol, const MxArgs a) {
   constexpr bool ROW = (MODE & MX_ROW) != 0;
   constexpr bool COL = (MODE & MX_COL) != 0;
   constexpr int OPERANDS = (ACT == ACT_SWIGLU) ? 2 : 1;
-  using L = MxLayout<WARPS, OPERANDS>;
+  using L = MxLayout<WARPS, OPERANDS, STAGES>;
   constexpr int THREADS = WARPS * 32;
   constexpr int BAND = L::BAND;
   constexpr int ROW_PITCH = MX_TILE_K * 2;   // bf16 tile row, bytes
@@ -145,7 +149,7 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int h = lane >> 4;     // which 16-row half of the warp's 32 rows
+  const int h = lane >> 4;     // which 8-row half of the warp's 16 rows
   const int c = lane & 15;     // which 8-column chunk
   const uint32_t bar0 = smem_addr(&full_bar[0]);
 
@@ -160,7 +164,7 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int t = t0 + j;
     const int band = t / a.tiles_k;
     const int tk = t - band * a.tiles_k;
-    const int s = j & 1;
+    const int s = j % STAGES;
     const uint32_t dst = sbase + s * L::STAGE_BYTES;
     mbar_arrive_expect_tx(bar0 + 8 * s, L::STAGE_BYTES);
     tma_load_2d(dst, &tmap_x, tk * MX_TILE_K, band * BAND, bar0 + 8 * s);
@@ -172,11 +176,10 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   if (tid == 0) {
     prefetch_tensormap(&tmap_x);
     if (COL) prefetch_tensormap(&tmap_qcol);
-    mbar_init(bar0, 1);
-    mbar_init(bar0 + 8, 1);
+#pragma unroll
+    for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
     fence_barrier_init();
-    issue_load(0);
-    if (count > 1) issue_load(1);
+    for (int jj = 0; jj < STAGES && jj < count; ++jj) issue_load(jj);
   }
   __syncthreads();
 
@@ -185,35 +188,34 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   int rsc_first = -1;          // first step slot gathered in the rowwise scale staging
 
   for (int j = 0; j < count; ++j) {
-    const int s = j & 1;
+    const int s = j % STAGES;
     const int t = t0 + j;
     const int band = t / a.tiles_k;
     const int tk = t - band * a.tiles_k;
-    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (j >> 1) & 1, a.timeout_ns);
+    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (j / STAGES) & 1, a.timeout_ns);
 
     const uint32_t my_row0 =
-        sbase + s * L::STAGE_BYTES + (32 * warp + 16 * h) * ROW_PITCH + c * 16;
+        sbase + s * L::STAGE_BYTES + (16 * warp + 8 * h) * ROW_PITCH + c * 16;
 
-    // ---- load this lane's 16 x 8 block and reduce it to magnitude maxima --
-    // y[i][jc]: the values to quantize (fp32).  ce[p] / re[q]: exponent
-    // fields of the largest magnitudes of columns 2p, 2p+1 / rows 2q, 2q+1,
-    // packed as two 16-bit lanes.
+    // ---- load this lane's 8 x 8 block and reduce it to magnitude maxima ---
     // The plain path keeps the packed bf16 pairs (xr) and widens them where
-    // they are used; the activation paths hold y in fp32.
-    uint32_t xr[ACT == ACT_NONE ? 16 : 1][4];
-    float y[ACT == ACT_NONE ? 1 : 16][8];
+    // they are used; the activation paths hold y in fp32.  ce[p] / re[q]:
+    // exponent fields of the largest magnitudes of columns 2p, 2p+1 / rows
+    // 2q, 2q+1, packed as two 16-bit lanes.
+    uint32_t xr[ACT == ACT_NONE ? 8 : 1][4];
+    float y[ACT == ACT_NONE ? 1 : 8][8];
     uint32_t ce[4] = {0u, 0u, 0u, 0u};
-    uint32_t re[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    uint32_t re[4] = {0u, 0u, 0u, 0u};
     if (ok) {
       if constexpr (ACT == ACT_NONE) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const uint4 v = lds128(my_row0 + i * ROW_PITCH);
           xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
         }
         uint32_t cm[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
+        for (int i = 0; i < 8; i += 2) {
           uint32_t tt[2];
 #pragma unroll
           for (int di = 0; di < 2; ++di) {
@@ -230,7 +232,7 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         for (int p = 0; p < 4; ++p) ce[p] = bf16_exponents(cm[p]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const uint4 v = lds128(my_row0 + i * ROW_PITCH);
           uint32_t u[4] = {0u, 0u, 0u, 0u};
           if constexpr (ACT == ACT_SWIGLU) {
@@ -250,9 +252,9 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
           }
         }
         uint32_t cmx[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        uint32_t rmx[16];
+        uint32_t rmx[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           rmx[i] = 0u;
 #pragma unroll
           for (int jc = 0; jc < 8; ++jc) {
@@ -262,42 +264,53 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
           }
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) re[q] = (rmx[2 * q] >> 23) | ((rmx[2 * q + 1] >> 23) << 16);
+        for (int q = 0; q < 4; ++q) re[q] = (rmx[2 * q] >> 23) | ((rmx[2 * q + 1] >> 23) << 16);
 #pragma unroll
         for (int p = 0; p < 4; ++p) ce[p] = (cmx[2 * p] >> 23) | ((cmx[2 * p + 1] >> 23) << 16);
       }
     }
+    // Column maxima over the warp's 16 rows, published for the partner warp
+    // that holds the other 16 rows of the same 32-row block.
+#pragma unroll
+    for (int p = 0; p < 4; ++p) ce[p] = vmax_u16x2(ce[p], __shfl_xor_sync(0xFFFFFFFFu, ce[p], 16));
+    const uint32_t xch = sbase + L::OFF_XCH + (warp * 16 + c) * 16;
+    if (COL && h == 0) sts128(xch, ce[0], ce[1], ce[2], ce[3]);
 
     // ---- barrier A: the slot has been read by every warp, the colwise
-    // staging is free (thread 0 waited for the previous store), and every
-    // thread knows whether the copy landed. -------------------------------
+    // staging is free (thread 0 waited for the previous store), the column
+    // maxima are published, and every thread knows whether the copy landed.
     fence_proxy_async_smem();
     if (COL && tid == 0) bulk_wait_read<0>();
     if (__syncthreads_or(!ok)) {
-      // A copy never landed: record it, let the other copy in flight and the
-      // pending stores finish (bounded), and stop without more output.
+      // A copy never landed: record it, let the other copies in flight and
+      // the pending stores finish (bounded), and stop without more output.
       if (tid == 0) {
         if (a.dev_err) atomicOr(a.dev_err, 1u);
-        if (j + 1 < count)
-          mbar_wait_bounded(bar0 + 8 * (s ^ 1), ((j + 1) >> 1) & 1, a.timeout_ns);
+        for (int jj = j + 1; jj < j + STAGES && jj < count; ++jj)
+          mbar_wait_bounded(bar0 + 8 * (jj % STAGES), (jj / STAGES) & 1, a.timeout_ns);
         bulk_wait_all();
       }
       return;
     }
-    if (tid == 0 && j + 2 < count) issue_load(j + 2);
+    if (tid == 0 && j + STAGES < count) issue_load(j + STAGES);
 
-    // ---- complete the block maxima across lanes -------------------------
+    // ---- complete the block maxima --------------------------------------
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 1));
       re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 2));
     }
-#pragma unroll
-    for (int p = 0; p < 4; ++p) ce[p] = vmax_u16x2(ce[p], __shfl_xor_sync(0xFFFFFFFFu, ce[p], 16));
+    if constexpr (COL) {
+      const uint4 other = lds128(sbase + L::OFF_XCH + ((warp ^ 1) * 16 + c) * 16);
+      ce[0] = vmax_u16x2(ce[0], other.x);
+      ce[1] = vmax_u16x2(ce[1], other.y);
+      ce[2] = vmax_u16x2(ce[2], other.z);
+      ce[3] = vmax_u16x2(ce[3], other.w);
+    }
 
     const int col0 = tk * MX_TILE_K + c * 8;            // first column of this lane
     const bool col_ok = col0 < a.K;
-    const int row0 = band * BAND + 32 * warp + 16 * h;  // first row of this lane
+    const int row0 = band * BAND + 16 * warp + 8 * h;   // first row of this lane
     const bool row_ok = row0 < a.M;
     const int slot = tk & 7;                            // rowwise scale gathering slot
 
@@ -312,12 +325,12 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
     // ---- rowwise: codes straight to global, scale bytes to staging --------
     if constexpr (ROW) {
-      uint32_t rc[8];
+      uint32_t rc[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) rc[q] = e8m0_pair(re[q]);
+      for (int q = 0; q < 4; ++q) rc[q] = e8m0_pair(re[q]);
       uint8_t* qrow = a.q_row + static_cast<size_t>(row0) * a.K + col0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 8; ++i) {
         const float inv = inv_scale_from_e8m0(half16(rc[i >> 1], i & 1));
         const float2 iv = make_float2(inv, inv);
         uint32_t w[4];
@@ -329,15 +342,13 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         if (col_ok && row_ok)
           stg64(qrow + static_cast<size_t>(i) * a.K, w[0] | (w[1] << 16), w[2] | (w[3] << 16));
       }
-      // Lane (h, c) holds block c/4's codes for its 16 rows; it stages rows
-      // 4t + (c & 3) into [BAND rows][8 slots][4 blocks].
+      // Lane (h, c) holds block c/4's codes for its 8 rows; it stages rows
+      // r and r + 4 (r = c & 3) into [BAND rows][8 slots][4 blocks].
       const int r = c & 3, b = c >> 2;
-      const uint32_t rs = sbase + L::OFF_RSC + (32 * warp + 16 * h) * 32 + slot * 4 + b;
-#pragma unroll
-      for (int t4 = 0; t4 < 4; ++t4) {
-        const uint32_t pair = (r >> 1) ? rc[2 * t4 + 1] : rc[2 * t4];
-        sts8(rs + (4 * t4 + r) * 32, (pair >> (16 * (r & 1))) & 0xFFu);
-      }
+      const uint32_t rs = sbase + L::OFF_RSC + (16 * warp + 8 * h + r) * 32 + slot * 4 + b;
+      const int sh = 16 * (r & 1);
+      sts8(rs, ((r >> 1 ? rc[1] : rc[0]) >> sh) & 0xFFu);
+      sts8(rs + 4 * 32, ((r >> 1 ? rc[3] : rc[2]) >> sh) & 0xFFu);
     }
 
     // ---- colwise: codes and scale bytes to staging -------------------------
@@ -345,56 +356,58 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
       uint32_t cc[4];
 #pragma unroll
       for (int p = 0; p < 4; ++p) cc[p] = e8m0_pair(ce[p]);
-      // Staging half (warp / 4) holds m = 128 * half + 0..127 as
+      // Staging half (warp / 8) holds m = 128 * half + 0..127 as
       // [k % 8][k / 8][128 m], the 16-byte chunk index xor-ed with (k / 8) % 8
-      // (the 128-byte swizzle of the store's tensor map).
-      const uint32_t qs = sbase + L::OFF_QCOL + (warp >> 2) * L::QCOL_HALF + c * 128 +
-                          ((((warp & 3) * 2 + h) ^ (c & 7)) << 4);
+      // (the 128-byte swizzle of the store's tensor map).  The lane's 8 rows
+      // are the h-th 8-byte half of chunk (warp % 8).
+      const uint32_t qs = sbase + L::OFF_QCOL + (warp >> 3) * L::QCOL_HALF + c * 128 +
+                          (((warp & 7) ^ (c & 7)) << 4) + 8 * h;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         const float2 iv = make_float2(inv_scale_from_e8m0(half16(cc[p], 0)),
                                       inv_scale_from_e8m0(half16(cc[p], 1)));
-        uint32_t we[8], wo[8];   // codes of columns 2p (even) and 2p+1 (odd), two rows each
+        uint32_t we[4], wo[4];   // codes of columns 2p (even) and 2p+1 (odd), two rows each
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
+        for (int i = 0; i < 8; i += 2) {
           const float2 r0 = mul_f32x2(pair_at(i, p), iv);
           const float2 r1 = mul_f32x2(pair_at(i + 1, p), iv);
           we[i / 2] = cvt_e4m3x2(r0.x, r1.x);
           wo[i / 2] = cvt_e4m3x2(r0.y, r1.y);
         }
-        sts128(qs + (2 * p) * 2048, we[0] | (we[1] << 16), we[2] | (we[3] << 16),
-               we[4] | (we[5] << 16), we[6] | (we[7] << 16));
-        sts128(qs + (2 * p + 1) * 2048, wo[0] | (wo[1] << 16), wo[2] | (wo[3] << 16),
-               wo[4] | (wo[5] << 16), wo[6] | (wo[7] << 16));
+        sts64(qs + (2 * p) * 2048, we[0] | (we[1] << 16), we[2] | (we[3] << 16));
+        sts64(qs + (2 * p + 1) * 2048, wo[0] | (wo[1] << 16), wo[2] | (wo[3] << 16));
       }
-      // Scale bytes: [128 columns][8 row blocks]; h = 0 writes columns 0-3,
-      // h = 1 columns 4-7 of the lane's chunk.
+      // Scale bytes: [128 columns][BAND / 32 blocks]; both warps of a block
+      // hold the same codes, the even one writes them (h = 0: columns 0-3,
+      // h = 1: columns 4-7 of the lane's chunk).
+      if ((warp & 1) == 0) {
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
-        sts8(sbase + L::OFF_CSC + (c * 8 + 4 * h + jj) * 8 + warp,
-             (pair >> (16 * (jj & 1))) & 0xFFu);
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
+          sts8(sbase + L::OFF_CSC + (c * 8 + 4 * h + jj) * 8 + (warp >> 1),
+               (pair >> (16 * (jj & 1))) & 0xFFu);
+        }
       }
     }
 
-    // ---- dbias: column sums of the warp's 32 rows, pairwise ----------------
+    // ---- dbias: column sums of the warp's 16 rows, pairwise ----------------
     if constexpr (DBIAS) {
 #pragma unroll
       for (int jc = 0; jc < 8; ++jc) {
-        float v[16];
+        float v[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const float2 pr = pair_at(i, jc >> 1);
           v[i] = (jc & 1) ? pr.y : pr.x;
         }
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
+        for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
-        const float s32 = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
+        const float s16 = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
         if (h == 0) {
           float* db = reinterpret_cast<float*>(smem + L::OFF_DB) + warp * MX_TILE_K + c * 8 + jc;
-          *db = s32;
+          *db = s16;
         }
       }
     }
@@ -411,14 +424,17 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                        band * BAND + 128 * half, tk * (MX_TILE_K / 8), 0);
         bulk_commit();
       }
-      // Colwise scale bytes: one run of the band's blocks per column.
-      if (tid < MX_TILE_K) {
-        const int k = tk * MX_TILE_K + tid;
+      // Colwise scale bytes: one run of the band's blocks per column; every
+      // warp writes 128 / WARPS columns so no warp lengthens the step.
+      constexpr int COLS_PER_WARP = MX_TILE_K / WARPS;
+      if (lane < COLS_PER_WARP) {
+        const int kc = warp * COLS_PER_WARP + lane;
+        const int k = tk * MX_TILE_K + kc;
         const int mb0 = band * (BAND / 32);
         const int nvalid = min(BAND / 32, nmb - mb0);
         if (k < a.K) {
           uint8_t* dst = a.s_col + static_cast<size_t>(k) * nmb + mb0;
-          const uint32_t src = sbase + L::OFF_CSC + tid * 8;
+          const uint32_t src = sbase + L::OFF_CSC + kc * 8;
           const uint32_t lo = lds32(src), hi = lds32(src + 4);
           if (BAND == 256 && nvalid == 8 && (nmb & 7) == 0) {
             stg64(dst, lo, hi);
@@ -437,12 +453,14 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
       const bool flush = (slot == 7) || (tk + 1 == a.tiles_k) || (j + 1 == count);
       if (flush) {
         // Rowwise scale bytes of steps rsc_first..slot of this group of eight:
-        // one 32-byte sector per row when all eight steps are present.
-        const int row = band * BAND + tid;
-        if (row < a.M) {
+        // one 32-byte sector per row when all eight steps are present.  Warp
+        // w writes the 16 rows it quantized.
+        const int rr = 16 * warp + lane;
+        const int row = band * BAND + rr;
+        if (lane < 16 && row < a.M) {
           const int kb0 = (tk - slot) * 4;   // first k-block of the group
           uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
-          const uint32_t src = sbase + L::OFF_RSC + tid * 32;
+          const uint32_t src = sbase + L::OFF_RSC + rr * 32;
           if (rsc_first == 0 && slot == 7 && (nkb & 7) == 0) {
             const uint4 lo = lds128(src), hi = lds128(src + 16);
             stg128(dst, lo.x, lo.y, lo.z, lo.w);
@@ -458,10 +476,13 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
 
     if constexpr (DBIAS) {
-      // The band's sum of each column: pairwise over the warps' 32-row sums.
-      if (tid < MX_TILE_K) {
-        const int k = tk * MX_TILE_K + tid;
-        const float* db = reinterpret_cast<const float*>(smem + L::OFF_DB) + tid;
+      // The band's sum of each column: pairwise over the warps' 16-row sums;
+      // warp w adds up 128 / WARPS columns.
+      constexpr int COLS_PER_WARP = MX_TILE_K / WARPS;
+      if (lane < COLS_PER_WARP) {
+        const int kc = warp * COLS_PER_WARP + lane;
+        const int k = tk * MX_TILE_K + kc;
+        const float* db = reinterpret_cast<const float*>(smem + L::OFF_DB) + kc;
         float v[WARPS];
 #pragma unroll
         for (int w = 0; w < WARPS; ++w) v[w] = db[w * MX_TILE_K];
@@ -491,22 +512,49 @@ __global__ void dbias_finalize_kernel(const float* __restrict__ ws, int bands, i
 // Launch configuration per variant
 // ---------------------------------------------------------------------------
 
-// Warps per CTA (= 32-row slices of a band); one CTA per SM.
+// Warps per CTA (= 16-row slices of a band) and ring slots; one CTA per
+// SM.  Overridable at build time for tuning sweeps.
+#ifndef MXQ_PLAIN_WARPS
+#define MXQ_PLAIN_WARPS 8
+#endif
+#ifndef MXQ_PLAIN_STAGES
+#define MXQ_PLAIN_STAGES 3
+#endif
+#ifndef MXQ_GELU_WARPS
+#define MXQ_GELU_WARPS 8
+#endif
+#ifndef MXQ_GELU_STAGES
+#define MXQ_GELU_STAGES 3
+#endif
+#ifndef MXQ_SWIGLU_WARPS
+#define MXQ_SWIGLU_WARPS 8
+#endif
+#ifndef MXQ_SWIGLU_STAGES
+#define MXQ_SWIGLU_STAGES 2
+#endif
 template <int ACT>
-struct MxConfig {
-  static constexpr int WARPS = 8;   // band of 256 rows, 64 KiB per slot
+struct MxConfig {   // plain / dbias: band of 16 * WARPS rows
+  static constexpr int WARPS = MXQ_PLAIN_WARPS;
+  static constexpr int STAGES = MXQ_PLAIN_STAGES;
 };
 template <>
-struct MxConfig<ACT_SWIGLU> {
-  static constexpr int WARPS = 4;   // band of 128 rows, gate + up = 64 KiB per slot
+struct MxConfig<ACT_GELU> {
+  static constexpr int WARPS = MXQ_GELU_WARPS;
+  static constexpr int STAGES = MXQ_GELU_STAGES;
+};
+template <>
+struct MxConfig<ACT_SWIGLU> {   // gate + up per slot
+  static constexpr int WARPS = MXQ_SWIGLU_WARPS;
+  static constexpr int STAGES = MXQ_SWIGLU_STAGES;
 };
 
 template <int MODE, bool DBIAS, int ACT>
 cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
                            cudaStream_t stream) {
   constexpr int WARPS = MxConfig<ACT>::WARPS;
-  using L = MxLayout<WARPS, ACT == ACT_SWIGLU ? 2 : 1>;
-  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS>;
+  constexpr int STAGES = MxConfig<ACT>::STAGES;
+  using L = MxLayout<WARPS, ACT == ACT_SWIGLU ? 2 : 1, STAGES>;
+  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS, STAGES>;
 
   static int configured_device = -1;
   int dev = 0;
@@ -536,7 +584,11 @@ cudaError_t launch_mode(const MxMaps& maps, const MxArgs& a, int mode, int num_s
 }  // namespace
 
 int mx_band_rows(int act) {
-  return 32 * (act == ACT_SWIGLU ? MxConfig<ACT_SWIGLU>::WARPS : MxConfig<ACT_NONE>::WARPS);
+  switch (act) {
+    case ACT_GELU: return 16 * MxConfig<ACT_GELU>::WARPS;
+    case ACT_SWIGLU: return 16 * MxConfig<ACT_SWIGLU>::WARPS;
+    default: return 16 * MxConfig<ACT_NONE>::WARPS;
+  }
 }
 
 cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
