@@ -99,6 +99,33 @@ def mx_quantize_rowcol(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_
     return out
 
 
+def mx_quantize_rowcol_dbias_noalloc(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None,
+                                     q_col=None, s_col=None, dbias=None, dev_err=None,
+                                     stream=None):
+    """mx_quantize_rowcol with dbias, for callers that cannot allocate a
+    workspace: the library keeps the band sums in its own fixed 8 MiB
+    device array (see include/mxq.h for the limit, and for ordering calls
+    that share it).  Outputs not passed in are allocated here with torch,
+    as in the other bindings; pass them all to allocate nothing."""
+    ldx = _input(x)
+    M, K = x.shape
+    dev = x.device
+    out = {}
+    if flags & ROWWISE:
+        out["q_row"] = q_row if q_row is not None else _empty((M, K), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty((M, K // 32), torch.uint8, dev)
+    if flags & COLWISE:
+        out["q_col"] = q_col if q_col is not None else _empty((K, M), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty((K, M // 32), torch.uint8, dev)
+    out["dbias"] = dbias if dbias is not None else _empty((K,), torch.float32, dev)
+    st = _lib.lib().mx_quantize_rowcol_dbias_noalloc(
+        _ptr(x), M, K, ldx, flags, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
+        _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(out["dbias"]), _ptr(dev_err),
+        _stream(stream))
+    _check(st, "mx_quantize_rowcol_dbias_noalloc")
+    return out
+
+
 def mx_quantize_gated(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_col=None,
                       s_col=None, dev_err=None, stream=None):
     """SwiGLU-gated MXFP8 of x[M, 2N] = [gate | up]; y = silu(gate) * up

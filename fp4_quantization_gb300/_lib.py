@@ -22,6 +22,8 @@ SIGNATURES = {
     "mxq_workspace_bytes": (_sz, [ctypes.c_int, _i64, _i64, _u32]),
     "mx_quantize_rowcol": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _sz, _vp, _vp]),
+    "mx_quantize_rowcol_dbias_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp,
+                                                        _vp, _vp, _vp, _vp, _vp]),
     "mx_quantize_gated": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _vp, _vp,
                                          _vp]),
     "bf16_amax": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp]),

@@ -120,6 +120,36 @@ MXQ_API mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64
                               uint32_t* dev_err, mxq_stream_t stream);
 
 /*
+ * mx_quantize_rowcol_dbias_noalloc -- mx_quantize_rowcol with MXQ_DBIAS for
+ * callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point.
+ *
+ * Some callers cannot provide the dbias workspace: code inside a framework
+ * that owns all device memory through its own pool (an extra cudaMalloc
+ * would bypass the pool and synchronise the device), loops that forbid
+ * allocation after start-up, and plugin hosts that pass this library only
+ * the tensors it reads and writes.  This entry point takes the same
+ * arguments as mx_quantize_rowcol minus the workspace, always computes
+ * dbias (MXQ_DBIAS is implied; MXQ_ACT_GELU_TANH is refused with
+ * MXQ_EINVAL), and keeps its scratch in a device array the library owns:
+ * 8 MiB, held on every GPU that loads the library until the process exits.
+ *   - Limit: shapes needing more than 8 MiB of band sums
+ *     (mxq_workspace_bytes(MXQ_OP_ROWCOL, M, K, MXQ_DBIAS) > 8 MiB, e.g.
+ *     more than 16384 x 16384) return MXQ_EWORKSPACE; nothing is enqueued.
+ *   - The first call made with a device current looks up the array's device
+ *     address; make that first call before any stream capture begins.
+ *   - All calls share the array.  Nothing in it needs clearing (every value
+ *     read is written earlier in the same call), but calls that overlap on
+ *     the GPU race on it: order them, e.g. on one stream.
+ *   - It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+MXQ_API mxq_status mx_quantize_rowcol_dbias_noalloc(const void* x, int64_t M, int64_t K,
+                                                    int64_t ldx, uint32_t flags, uint8_t* q_row,
+                                                    uint8_t* s_row, uint8_t* q_col,
+                                                    uint8_t* s_col, float* dbias,
+                                                    uint32_t* dev_err, mxq_stream_t stream);
+
+/*
  * mx_quantize_gated -- SwiGLU gate fused with MXFP8 quantization.
  *
  * Operation: y[m][n] = silu(x[m][n]) * x[m][N + n] for n < N, silu(g) =
