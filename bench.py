@@ -233,8 +233,9 @@ def time_device(fn, steps, warmup, world, stream):
     return total, per_call, max_over_ranks(total, world)
 
 
-def rows_measurements(mxq, device, steps, warmup, world, stream, peak):
-    """The other hot-path variants, each on its own workload."""
+def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None):
+    """The other hot-path variants, each on its own workload (only the one
+    named `only` when given)."""
     out = {}
     cases = [
         ("dim1_colwise_16384x16384", lambda: synth.dim1(),
@@ -252,14 +253,24 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak):
         ("nvfp4_rowtrans_16384x8192", lambda: synth.nvfp4(),
          lambda x, o: mxq.nvfp4_quantize_transpose(x, mxq.ROWWISE | mxq.COLWISE, **o),
          nvfp4_bytes(16384, 8192), {}),
+        ("nvfp4_rowtrans_given_amax_16384x8192", lambda: synth.nvfp4(),
+         lambda x, o: mxq.nvfp4_quantize_transpose(x, mxq.ROWWISE | mxq.COLWISE, **o),
+         nvfp4_bytes(16384, 8192), {}),
+        ("bf16_amax_16384x8192", lambda: synth.nvfp4(),
+         lambda x, o: mxq.bf16_amax(x, **o), 16384 * 8192 * 2 + 4, {}),
     ]
     for name, gen, call, nbytes, _ in cases:
+        if only is not None and name != only:
+            continue
         x = to_device(gen(), device)
         first = call(x, {})                       # allocates the outputs once
-        keep = {k: v for k, v in first.items() if k != "dbias"}
-        if "dbias" in first:
-            keep["dbias"] = first["dbias"]
-        if name.startswith("nvfp4"):
+        if name.startswith("bf16_amax"):
+            keep = {"out": first}
+        else:
+            keep = dict(first)
+        if name.startswith("nvfp4_rowtrans_given_amax"):
+            keep["amax"] = mxq.bf16_amax(x)
+        elif name.startswith("nvfp4"):
             keep["workspace"] = torch.empty(16, dtype=torch.uint8, device=device)
         if name.startswith("dbias"):
             keep["workspace"] = torch.empty(
@@ -268,13 +279,15 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak):
         total, per_call, _ = time_device(lambda: call(x, keep), steps, warmup, world, stream)
         avg_ms = total / steps
         gbs = nbytes / (avg_ms * 1e-3) / 1e9
-        launches = 2 if (name.startswith("dbias") or name.startswith("nvfp4")) else 1
+        launches = 2 if (name.startswith("dbias") or name.startswith("nvfp4_rowtrans_16")) else 1
         out[name] = {"GB_per_s": round(gbs, 1), "us_per_call": round(avg_ms * 1e3, 2),
                      "bytes_per_call": nbytes, "frac_of_hbm_peak": round(gbs / peak, 4),
                      "launches_per_call": launches}
-        if name.startswith("nvfp4"):
+        if name.startswith("nvfp4_rowtrans_16"):
             out[name]["note"] = ("bytes exclude the tensor-amax pass (a second 256 MiB read), "
                                  "time includes it")
+        if name.startswith("nvfp4_rowtrans_given"):
+            out[name]["note"] = "tensor amax supplied by the caller: the quantize kernel alone"
         del x, first, keep
         torch.cuda.empty_cache()
     return out
@@ -335,6 +348,13 @@ def gpu_arm(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
     peak, peak_kind = measured_peaks()
+    if args.only:
+        # One hot-path variant alone (profiling runs); no headline line.
+        rows = rows_measurements(mxq, device, args.steps, args.warmup, world, stream, peak,
+                                 only=args.only)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "rows": rows}), flush=True)
+        return
     M, K = args.M, args.K
     bits = synth.rowcol(M=M, K=K)
     x = to_device(bits, device)
@@ -453,6 +473,8 @@ def main():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=4096)
+    p.add_argument("--only", default=None,
+                   help="time just this variant of the 'rows' object (profiling runs)")
     p.add_argument("--M", type=int, default=16384,
                    help="rows of the timed cast (16384 for the headline number)")
     p.add_argument("--K", type=int, default=16384, help="columns of the timed cast")

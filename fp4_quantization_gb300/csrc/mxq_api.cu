@@ -96,6 +96,30 @@ mxq_status encode_mx_qcol_map(CUtensorMap* map, int64_t M, int64_t K, uint8_t* q
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// NVFP4 code maps: rowwise [M][K/2] seen as [m % 8][m / 8][k / 2] (box
+// 128 B x band / 8 x 8) and transposed [K][M/2] seen as [k % 8][k / 8][m / 2]
+// (box 128 B x step / 8 x 8), both with the 128-byte swizzle.
+mxq_status encode_nv_code_maps(mxq::NvMaps* maps, uint32_t flags, int64_t M, int64_t K,
+                               uint8_t* q_row, uint8_t* q_t) {
+  if (flags & MXQ_ROWWISE) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M / 8), 8};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * K), static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(mxq::nv_band_rows() / 8), 8};
+    mxq_status st = encode_map(&maps->q_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q_row, dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != MXQ_OK) return st;
+  }
+  if (flags & MXQ_COLWISE) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(M / 2), static_cast<cuuint64_t>(K / 8), 8};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * M), static_cast<cuuint64_t>(M / 2)};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(mxq::nv_step_cols() / 8), 8};
+    mxq_status st = encode_map(&maps->q_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q_t, dims, strides,
+                               box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != MXQ_OK) return st;
+  }
+  return MXQ_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 mxq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA; }
@@ -267,7 +291,7 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE)) return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if (M < 0 || K < 0 || ldx < K) return MXQ_ESHAPE;
-  if ((M % 16) || (K % 16)) return MXQ_ESHAPE;
+  if ((M % 32) || (K % 32)) return MXQ_ESHAPE;
   if (M > (int64_t(1) << 30) || K > (int64_t(1) << 30) || M * K > (int64_t(1) << 40))
     return MXQ_ESHAPE;
   if (!global_scale) return MXQ_EINVAL;
@@ -298,11 +322,13 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
     if (st != MXQ_OK) return st;
     amax = ws_amax;
   }
+  const int band = mxq::nv_band_rows();
+  const int step = mxq::nv_step_cols();
   mxq::NvArgs a{};
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
-  a.tiles_m = static_cast<int>((M + mxq::NV_TILE_M - 1) / mxq::NV_TILE_M);
-  a.tiles_k = static_cast<int>((K + mxq::NV_TILE_K - 1) / mxq::NV_TILE_K);
+  a.tiles_m = static_cast<int>((M + band - 1) / band);
+  a.tiles_k = static_cast<int>((K + step - 1) / step);
   a.amax = amax;
   a.global_scale = global_scale;
   a.q_row = q_row;
@@ -311,10 +337,12 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   a.s_t = s_t;
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
-  CUtensorMap map;
-  st = encode_bf16_map(&map, x, M, K, ldx, mxq::NV_TILE_K, mxq::NV_TILE_M);
+  mxq::NvMaps maps{};
+  st = encode_bf16_map(&maps.x, x, M, K, ldx, step, band);
   if (st != MXQ_OK) return st;
-  return from_cuda(mxq::launch_nvfp4(map, a, direction_mode(flags), sms, stream));
+  st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t);
+  if (st != MXQ_OK) return st;
+  return from_cuda(mxq::launch_nvfp4(maps, a, direction_mode(flags), sms, stream));
 }
 
 mxq_status mxq_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* dev_err, mxq_stream_t stream) {

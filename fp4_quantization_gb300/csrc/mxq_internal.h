@@ -14,10 +14,6 @@ namespace mxq {
 constexpr int MX_TILE_M = 32;
 constexpr int MX_TILE_K = 128;
 
-// NVFP4 warp tile: 64 x 64 bf16 = 8 KiB (four 16-row transposed blocks per
-// column, four 1x16 row blocks per row).
-constexpr int NV_TILE_M = 64;
-constexpr int NV_TILE_K = 64;
 
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000000000ull;   // 1 s per wait
 
@@ -45,9 +41,19 @@ struct MxMaps {
   CUtensorMap q_col;
 };
 
+// TMA descriptors of one NVFP4 call: the bf16 input (box 64 columns x
+// nv_band_rows() rows), the rowwise codes [M][K/2] seen as
+// [m % 8][m / 8][k / 2] and the transposed codes [K][M/2] seen as
+// [k % 8][k / 8][m / 2] (both 128-byte swizzle).
+struct NvMaps {
+  CUtensorMap x;
+  CUtensorMap q_row;
+  CUtensorMap q_t;
+};
+
 struct NvArgs {
   int M, K;
-  int tiles_m, tiles_k;     // NV_TILE_M x NV_TILE_K tiles
+  int tiles_m, tiles_k;     // bands of nv_band_rows() rows, nv_step_cols() columns
   const float* amax;        // device tensor amax
   float* global_scale;      // device, receives amax / 2688
   uint8_t* q_row;
@@ -65,7 +71,9 @@ cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias,
                       int num_sms, cudaStream_t stream);
 cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
                                   cudaStream_t stream);
-cudaError_t launch_nvfp4(const CUtensorMap& map, const NvArgs& a, int mode, int num_sms,
+int nv_band_rows();
+int nv_step_cols();
+cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, int num_sms,
                          cudaStream_t stream);
 cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,
                              int num_sms, cudaStream_t stream);

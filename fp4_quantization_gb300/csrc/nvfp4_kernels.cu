@@ -7,15 +7,32 @@
 // 1D kernel named in its "Patched but not measurable" section); this file
 // implements the 1D (1x16 block) variant.
 //
-// Same pipeline shape as the MXFP8 kernels: one TMA ring per warp, 64 x 64
-// bf16 tiles (8 KiB).  Lane (h, c) = (lane / 8, lane % 8) owns rows
-// 16h..16h+15 and columns 8c..8c+7, so each transposed 16x1 block lies
-// entirely in one lane and each 1x16 row block in a lane pair.  Per block the
-// scale arithmetic runs in IEEE fp32 with explicit rounding intrinsics in
-// the fixed order (b / 6) / G -> E4M3 -> value * G -> 1 / d; each element
-// then takes one multiply by that reciprocal (no per-element division, as
-// in torchao PR #12 "Multiply with inverse scale in loop instead of
-// dividing", rationale) and cvt.rn.satfinite.e2m1x2.f32.
+// Layout of the work (same principles as the MXFP8 kernel: every output
+// leaves in whole lines or sectors, because the write side costs by L2
+// request, not by byte):
+//  * One CTA (8 warps, one CTA per SM) walks a contiguous range of steps; a
+//    step is a band of 256 rows x 64 columns (32 KiB of bf16) from a 3-slot
+//    TMA ring.  Steps run along K inside a band.
+//  * Warp w owns rows 32w..32w+31; lane (h, c) = (lane / 8, lane % 8) owns
+//    rows 8h..8h+7 and columns 8c..8c+7 of those (eight conflict-free
+//    16-byte shared loads).  A 1x16 row block spans lanes c = 2b, 2b+1 and a
+//    16x1 transposed block spans lanes h = 2g, 2g+1: one xor shuffle each.
+//  * Each block scale is computed once: the two lanes of a pair split the
+//    rows (or columns) and swap the reciprocals with one shuffle.  The scale
+//    arithmetic is IEEE fp32 with explicit rounding intrinsics in the fixed
+//    order (b / 6) / G -> E4M3 -> value * G -> 1 / d; each element then
+//    takes one multiply by that reciprocal (two per mul.rn.f32x2; no
+//    per-element division, as in torchao PR #12 "Multiply with inverse
+//    scale in loop instead of dividing", rationale) and
+//    cvt.rn.satfinite.e2m1x2.f32.
+//  * Transposed codes of a step (64 k-rows x 128 bytes) leave through one
+//    3-D TMA store over [K][M/2] seen as [k % 8][k / 8][m / 2] with 128-byte
+//    swizzle; rowwise codes of four steps (256 rows x 128 bytes) leave
+//    through one 3-D TMA store over [M][K/2] seen as [m % 8][m / 8][k / 2].
+//    Both layouts keep the shared-memory stores free of bank conflicts.
+//  * Rowwise scale bytes of eight steps are gathered into one 32-byte
+//    sector per row; transposed scale bytes leave as 16 bytes per column
+//    per step.
 
 #include <cfloat>
 
@@ -27,15 +44,21 @@ namespace {
 
 constexpr int NV_WARPS = 8;
 constexpr int NV_STAGES = 3;
+constexpr int NV_BAND = 32 * NV_WARPS;            // 256 rows per step
+constexpr int NV_STEP_K = 64;                     // columns per step
+constexpr int NV_STAGE_BYTES = NV_BAND * NV_STEP_K * 2;          // 32 KiB
+constexpr int NV_OFF_QT = NV_STAGES * NV_STAGE_BYTES;            // [8][8][128 B]
+constexpr int NV_OFF_QR = NV_OFF_QT + NV_STEP_K * NV_BAND / 2;   // [8][32][128 B]
+constexpr int NV_OFF_RSC = NV_OFF_QR + NV_BAND * 128;            // [256 rows][8 slots][4]
+constexpr int NV_OFF_TSC = NV_OFF_RSC + NV_BAND * 32;            // [64 cols][16 blocks]
+constexpr int NV_OFF_INV = NV_OFF_TSC + NV_STEP_K * 16;          // [128] fp32 1/d per code
+constexpr int NV_TAB_BINADES = 21;                               // code table: binades kept
+constexpr int NV_OFF_CODE = NV_OFF_INV + 128 * 4;                // [21 x 128] E4M3 codes
+constexpr int NV_SMEM = NV_OFF_CODE + NV_TAB_BINADES * 128 + 1024;   // + alignment pad
 
-struct NvSchedule {
-  int count, first, step, tiles_k;
-  __device__ void coords(int j, int& tm, int& tk) const {
-    const int t = first + j * step;
-    tm = t / tiles_k;
-    tk = t - tm * tiles_k;
-  }
-};
+__device__ __forceinline__ void bar_sync_nv() {
+  asm volatile("bar.sync 1, %0;" :: "r"(NV_WARPS * 32) : "memory");
+}
 
 // Block scale of one NVFP4 block from its amax b (exact fp32).
 __device__ __forceinline__ void nv_block_scale(float b, float G, uint32_t& code, float& inv) {
@@ -51,181 +74,348 @@ __device__ __forceinline__ void nv_block_scale(float b, float G, uint32_t& code,
   }
 }
 
+// One bf16 magnitude of a packed pair of maxima, as its 15 magnitude bits
+// (the sign bit left by max.xorsign.abs carries no meaning and is dropped).
+// 1 / (value(code) * G) as nv_block_scale computes it (0 for code 0 or a
+// zero product, the largest finite float if the reciprocal overflows).
+__device__ __forceinline__ float nv_inv_from_code(uint32_t code, float G) {
+  const float d = __fmul_rn(e4m3_to_f32(code), G);
+  if (code == 0u || d == 0.0f) return 0.0f;
+  const float inv = __frcp_rn(d);
+  return isinf(inv) ? FLT_MAX : inv;
+}
+
+__device__ __forceinline__ uint32_t mag16(uint32_t pair, int which) {
+  return (pair >> (16 * which)) & 0x7FFFu;
+}
+
+// Scale code of a block and the reciprocal its elements are multiplied by.
+// With G fixed for the tensor, the code depends only on the block amax b and
+// 1/d only on the code, so both come from per-CTA tables filled with the
+// exact arithmetic of nv_block_scale: codes for the NV_TAB_BINADES binades
+// of bf16 magnitudes at and below the tensor amax (anything smaller gives
+// b / (6 G) below 2^-10, i.e. code 0), reciprocals for the 127 positive
+// codes.  A block amax above the table (possible only when the caller's
+// amax is smaller than the data) takes the direct computation.
+struct NvScaleTables {
+  uint32_t code_tab, inv_tab;   // shared addresses
+  uint32_t lo_bits, hi_bits;    // magnitude bits covered: [lo_bits, hi_bits]
+  float G;
+
+  __device__ __forceinline__ void lookup(uint32_t mag, uint32_t& code, float& inv) const {
+    if (mag > hi_bits) {
+      nv_block_scale(__uint_as_float(mag << 16), G, code, inv);
+      return;
+    }
+    code = mag >= lo_bits ? ld_shared_u8(code_tab + (mag - lo_bits)) : 0u;
+    inv = __uint_as_float(lds32(inv_tab + 4 * code));
+  }
+};
+
+// Swizzled byte offset inside a [rows][128 B] staging block whose TMA map
+// uses the 128-byte swizzle: the 16-byte chunk index is xor-ed with the
+// row index modulo 8.
+__device__ __forceinline__ uint32_t swz128(int row, int byte) {
+  return row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NV_WARPS * 32, 1)
-nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap, const NvArgs a) {
+nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                      const __grid_constant__ CUtensorMap tmap_qrow,
+                      const __grid_constant__ CUtensorMap tmap_qt, const NvArgs a) {
   constexpr bool ROW = (MODE & MX_ROW) != 0;
   constexpr bool COL = (MODE & MX_COL) != 0;
-  constexpr int STAGE_BYTES = NV_TILE_M * NV_TILE_K * 2;
-  constexpr int ROW_PITCH = NV_TILE_K * 2;
+  constexpr int ROW_PITCH = NV_STEP_K * 2;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[NV_WARPS][NV_STAGES];
-  __shared__ __align__(16) uint32_t row_scale_stage[NV_WARPS][64];
+  __shared__ __align__(8) uint64_t full_bar[NV_STAGES];
 
-  uint8_t* smem = align_up_shared<128>(smem_raw);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int h = lane >> 3;   // 16-row group 0..3
+  uint8_t* smem = align_up_shared<1024>(smem_raw);
+  const uint32_t sbase = smem_addr(smem);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int h = lane >> 3;   // 8-row group 0..3 of the warp's 32 rows
   const int c = lane & 7;    // 8-column chunk 0..7
-  const uint32_t stage0 = smem_addr(smem) + warp * NV_STAGES * STAGE_BYTES;
-  const uint32_t bar0 = smem_addr(&bars[warp][0]);
-  const uint32_t rs_stage = smem_addr(&row_scale_stage[warp][0]);
+  const uint32_t bar0 = smem_addr(&full_bar[0]);
 
   const float A = *a.amax;
   const float G = __fdiv_rn(A, 2688.0f);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.global_scale = G;
+  if (blockIdx.x == 0 && tid == 0) *a.global_scale = G;
 
-  NvSchedule sched;
-  const int gw = blockIdx.x * NV_WARPS + warp;
-  const int W = gridDim.x * NV_WARPS;
-  const int total = a.tiles_m * a.tiles_k;
-  sched.first = gw;
-  sched.step = W;
-  sched.tiles_k = a.tiles_k;
-  sched.count = gw < total ? (total - gw + W - 1) / W : 0;
-  if (sched.count == 0) return;
-
-  if (lane == 0) {
-    prefetch_tensormap(&tmap);
-#pragma unroll
-    for (int s = 0; s < NV_STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
-    fence_barrier_init();
+  // Scale tables (see NvScaleTables).
+  NvScaleTables tabs;
+  tabs.G = G;
+  tabs.code_tab = sbase + NV_OFF_CODE;
+  tabs.inv_tab = sbase + NV_OFF_INV;
+  {
+    const int ea = static_cast<int>((__float_as_uint(A) >> 23) & 0xFFu);
+    const int lo_e = ea > NV_TAB_BINADES - 1 ? ea - (NV_TAB_BINADES - 1) : 0;
+    tabs.lo_bits = static_cast<uint32_t>(lo_e) << 7;
+    tabs.hi_bits = (static_cast<uint32_t>(ea) << 7) | 0x7Fu;
+    const int entries = static_cast<int>(tabs.hi_bits - tabs.lo_bits) + 1;
+    for (int e = tid; e < entries; e += NV_WARPS * 32) {
+      uint32_t code;
+      float inv;
+      nv_block_scale(__uint_as_float((tabs.lo_bits + e) << 16), G, code, inv);
+      sts8(tabs.code_tab + e, code);
+    }
+    for (int cd = tid; cd < 128; cd += NV_WARPS * 32)
+      sts32(tabs.inv_tab + 4 * cd, __float_as_uint(nv_inv_from_code(cd, G)));
   }
-  __syncwarp();
 
-  auto issue = [&](int j) {
-    int tm, tk;
-    sched.coords(j, tm, tk);
+  const int64_t total = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
+  const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
+  const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
+  const int count = t1 - t0;
+  if (count <= 0) return;
+
+  auto issue_load = [&](int j) {   // thread 0 only
+    const int t = t0 + j;
+    const int band = t / a.tiles_k;
+    const int tk = t - band * a.tiles_k;
     const int s = j % NV_STAGES;
-    mbar_arrive_expect_tx(bar0 + 8 * s, STAGE_BYTES);
-    tma_load_2d(stage0 + s * STAGE_BYTES, &tmap, tk * NV_TILE_K, tm * NV_TILE_M, bar0 + 8 * s);
+    mbar_arrive_expect_tx(bar0 + 8 * s, NV_STAGE_BYTES);
+    tma_load_2d(sbase + s * NV_STAGE_BYTES, &tmap_x, tk * NV_STEP_K, band * NV_BAND, bar0 + 8 * s);
   };
-  if (lane == 0) {
-    const int pre = sched.count < NV_STAGES ? sched.count : NV_STAGES;
-    for (int j = 0; j < pre; ++j) issue(j);
-  }
 
-  for (int j = 0; j < sched.count; ++j) {
+  if (tid == 0) {
+    prefetch_tensormap(&tmap_x);
+    if (ROW) prefetch_tensormap(&tmap_qrow);
+    if (COL) prefetch_tensormap(&tmap_qt);
+#pragma unroll
+    for (int st = 0; st < NV_STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_barrier_init();
+    for (int jj = 0; jj < NV_STAGES && jj < count; ++jj) issue_load(jj);
+  }
+  __syncthreads();
+
+  const int nkb = a.K / 16;   // rowwise scale bytes per row
+  const int nmb = a.M / 16;   // transposed scale bytes per column
+  int rq_first = -1;          // first slot of the rowwise code group gathered
+  int rs_first = -1;          // first slot of the rowwise scale group gathered
+
+  for (int j = 0; j < count; ++j) {
     const int s = j % NV_STAGES;
+    const int t = t0 + j;
+    const int band = t / a.tiles_k;
+    const int tk = t - band * a.tiles_k;
     const bool ok = mbar_wait_bounded(bar0 + 8 * s, (j / NV_STAGES) & 1, a.timeout_ns);
-    if (__any_sync(0xFFFFFFFFu, !ok)) {
-      if (lane == 0 && a.dev_err) atomicOr(a.dev_err, 1u);
-      const int last = (j + NV_STAGES < sched.count) ? j + NV_STAGES : sched.count;
-      for (int jj = j + 1; jj < last; ++jj)
-        mbar_wait_bounded(bar0 + 8 * (jj % NV_STAGES), (jj / NV_STAGES) & 1, a.timeout_ns);
+
+    // ---- load this lane's 8 x 8 block; magnitude maxima ---------------------
+    const uint32_t my_row0 = sbase + s * NV_STAGE_BYTES + (32 * warp + 8 * h) * ROW_PITCH + c * 16;
+    uint32_t xr[8][4];
+    uint32_t cm[4] = {0u, 0u, 0u, 0u};   // columns 2p / 2p+1 over the lane's 8 rows
+    uint32_t rm[4] = {0u, 0u, 0u, 0u};   // rows 2q / 2q+1 over the lane's 8 columns
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = lds128(my_row0 + i * ROW_PITCH);
+        xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        uint32_t tt[2];
+#pragma unroll
+        for (int di = 0; di < 2; ++di) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], xr[i + di][p]);
+          tt[di] = absmax_bf16x2(absmax_bf16x2(xr[i + di][0], xr[i + di][1]),
+                                 absmax_bf16x2(xr[i + di][2], xr[i + di][3]));
+        }
+        rm[i / 2] = absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632));
+      }
+    }
+
+    // ---- barrier A: slot read by all warps, code staging free ---------------
+    fence_proxy_async_smem();
+    if (tid == 0) bulk_wait_read<0>();
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        if (a.dev_err) atomicOr(a.dev_err, 1u);
+        for (int jj = j + 1; jj < j + NV_STAGES && jj < count; ++jj)
+          mbar_wait_bounded(bar0 + 8 * (jj % NV_STAGES), (jj / NV_STAGES) & 1, a.timeout_ns);
+        bulk_wait_all();
+      }
       return;
     }
-    int tm, tk;
-    sched.coords(j, tm, tk);
-    const uint32_t my_row0 = stage0 + s * STAGE_BYTES + (16 * h) * ROW_PITCH + c * 16;
+    if (tid == 0 && j + NV_STAGES < count) issue_load(j + NV_STAGES);
 
-    uint32_t xr[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint4 v = lds128(my_row0 + i * ROW_PITCH);
-      xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
-    }
-    // cm[p]: magnitude maxima of columns 2p / 2p+1 over this lane's 16 rows
-    // (complete transposed blocks).  rm[q]: rows 2q / 2q+1 over 8 columns.
-    uint32_t cm[4] = {0u, 0u, 0u, 0u};
-    uint32_t rm[8];
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      uint32_t t[2];
-#pragma unroll
-      for (int di = 0; di < 2; ++di) {
-        const uint32_t a0 = xr[i + di][0] & 0x7FFF7FFFu;
-        const uint32_t a1 = xr[i + di][1] & 0x7FFF7FFFu;
-        const uint32_t a2 = xr[i + di][2] & 0x7FFF7FFFu;
-        const uint32_t a3 = xr[i + di][3] & 0x7FFF7FFFu;
-        cm[0] = vmax_u16x2(cm[0], a0);
-        cm[1] = vmax_u16x2(cm[1], a1);
-        cm[2] = vmax_u16x2(cm[2], a2);
-        cm[3] = vmax_u16x2(cm[3], a3);
-        t[di] = vmax_u16x2(vmax_u16x2(a0, a1), vmax_u16x2(a2, a3));
-      }
-      rm[i / 2] = vmax_u16x2(prmt(t[0], t[1], 0x5410), prmt(t[0], t[1], 0x7632));
-    }
-
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && j + NV_STAGES < sched.count) issue(j + NV_STAGES);
-
-    const int col0 = tk * NV_TILE_K + c * 8;
-    const int row0 = tm * NV_TILE_M + 16 * h;
+    const int col0 = tk * NV_STEP_K + 8 * c;
+    const int row0 = band * NV_BAND + 32 * warp + 8 * h;
     const bool col_ok = col0 < a.K;
     const bool row_ok = row0 < a.M;
 
+    // The lane's values widened to fp32 once, for both directions.
+    float2 xv[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) xv[i][p] = make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p]));
+    auto pair_at = [&](int i, int p) -> float2 { return xv[i][p]; };
+
+    // ---- rowwise: block scales (split over the c pair), codes, scale bytes --
     if constexpr (ROW) {
-      // 1x16 row blocks span lanes c = 2b, 2b+1.
 #pragma unroll
-      for (int q = 0; q < 8; ++q) rm[q] = vmax_u16x2(rm[q], __shfl_xor_sync(0xFFFFFFFFu, rm[q], 1));
-      uint8_t* qrow = a.q_row + static_cast<size_t>(row0) * (a.K / 2) + col0 / 2;
-      uint32_t codes[16];
+      for (int q = 0; q < 4; ++q) rm[q] = absmax_bf16x2(rm[q], __shfl_xor_sync(0xFFFFFFFFu, rm[q], 1));
+      const int mine = c & 1;               // this lane scales rows 4*mine .. 4*mine+3
+      uint32_t rcode[4];
+      float rinv_own[4], rinv_oth[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float b = __uint_as_float(((rm[i >> 1] >> (16 * (i & 1))) & 0xFFFFu) << 16);
-        float inv;
-        nv_block_scale(b, G, codes[i], inv);
-        const uint32_t w = cvt_e2m1x8(
-            bf16_lo(xr[i][0]) * inv, bf16_hi(xr[i][0]) * inv, bf16_lo(xr[i][1]) * inv,
-            bf16_hi(xr[i][1]) * inv, bf16_lo(xr[i][2]) * inv, bf16_hi(xr[i][2]) * inv,
-            bf16_lo(xr[i][3]) * inv, bf16_hi(xr[i][3]) * inv);
-        if (col_ok && row_ok) stg32(qrow + static_cast<size_t>(i) * (a.K / 2), w);
+      for (int tq = 0; tq < 4; ++tq) {
+        const uint32_t pair = mine ? rm[2 + (tq >> 1)] : rm[tq >> 1];
+        tabs.lookup(mag16(pair, tq & 1), rcode[tq], rinv_own[tq]);
       }
-      // Scale bytes: lanes c = 2b (rows i even) and 2b+1 (rows i odd) stage
-      // block b of their rows into [64 rows][4 blocks]; lane L then writes
-      // rows 2L and 2L+1.
-      const int b = c >> 1, r = c & 1;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const uint32_t code = r ? codes[i + 1] : codes[i];
-        sts8(rs_stage + (16 * h + i + r) * 4 + b, code);
+      for (int tq = 0; tq < 4; ++tq) rinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, rinv_own[tq], 1);
+      float rinv[8];
+#pragma unroll
+      for (int tq = 0; tq < 4; ++tq) {
+        rinv[tq] = mine ? rinv_oth[tq] : rinv_own[tq];
+        rinv[4 + tq] = mine ? rinv_own[tq] : rinv_oth[tq];
       }
-      __syncwarp();
-      const int nkb = a.K / 16;
-      const int kb0 = tk * (NV_TILE_K / 16);
-      const int valid = min(4, nkb - kb0);
+      // Codes of row i: 8 values -> 4 bytes at k / 2 = 4c within this step.
+      const int slot4 = tk & 3;
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int tr = 2 * lane + rr;
-        const int grow = tm * NV_TILE_M + tr;
-        const uint32_t w = lds32(rs_stage + tr * 4);
-        if (grow < a.M) {
-          uint8_t* srow = a.s_row + static_cast<size_t>(grow) * nkb + kb0;
-          if (valid == 4 && (nkb & 3) == 0) {
-            stg32(srow, w);
+      for (int i = 0; i < 8; ++i) {
+        const float2 iv = make_float2(rinv[i], rinv[i]);
+        const float2 v0 = mul_f32x2(pair_at(i, 0), iv);
+        const float2 v1 = mul_f32x2(pair_at(i, 1), iv);
+        const float2 v2 = mul_f32x2(pair_at(i, 2), iv);
+        const float2 v3 = mul_f32x2(pair_at(i, 3), iv);
+        const uint32_t w = cvt_e2m1x8(v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y);
+        // staging [m % 8][m / 8][128 B]: row index i * 32 + (4 * warp + h)
+        const int srow = i * 32 + 4 * warp + h;
+        sts32(sbase + NV_OFF_QR + swz128(srow, slot4 * 32 + 4 * c), w);
+      }
+      // Scale bytes: [256 rows][8 slots][4 blocks of 16 columns].
+      const int slot8 = tk & 7;
+#pragma unroll
+      for (int tq = 0; tq < 4; ++tq)
+        sts8(sbase + NV_OFF_RSC + (32 * warp + 8 * h + 4 * mine + tq) * 32 + slot8 * 4 + (c >> 1),
+             rcode[tq]);
+    }
+
+    // ---- transposed: block scales (split over the h pair), codes, scales ----
+    if constexpr (COL) {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], __shfl_xor_sync(0xFFFFFFFFu, cm[p], 8));
+      const int mine = h & 1;               // this lane scales columns 4*mine .. 4*mine+3
+      uint32_t tcode[4];
+      float tinv_own[4], tinv_oth[4];
+#pragma unroll
+      for (int tq = 0; tq < 4; ++tq) {
+        const uint32_t pair = mine ? cm[2 + (tq >> 1)] : cm[tq >> 1];
+        tabs.lookup(mag16(pair, tq & 1), tcode[tq], tinv_own[tq]);
+      }
+#pragma unroll
+      for (int tq = 0; tq < 4; ++tq) tinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, tinv_own[tq], 8);
+      float tinv[8];
+#pragma unroll
+      for (int tq = 0; tq < 4; ++tq) {
+        tinv[tq] = mine ? tinv_oth[tq] : tinv_own[tq];
+        tinv[4 + tq] = mine ? tinv_own[tq] : tinv_oth[tq];
+      }
+      // Codes of column jc: 8 rows -> 4 bytes at m / 2 = 16 * warp + 4h.
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 iv = make_float2(tinv[2 * p], tinv[2 * p + 1]);
+        float2 r[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[i] = mul_f32x2(pair_at(i, p), iv);
+        const uint32_t we = cvt_e2m1x8(r[0].x, r[1].x, r[2].x, r[3].x, r[4].x, r[5].x, r[6].x, r[7].x);
+        const uint32_t wo = cvt_e2m1x8(r[0].y, r[1].y, r[2].y, r[3].y, r[4].y, r[5].y, r[6].y, r[7].y);
+        // staging [k % 8][k / 8][128 B]: row index jc * 8 + c
+        sts32(sbase + NV_OFF_QT + swz128((2 * p) * 8 + c, 16 * warp + 4 * h), we);
+        sts32(sbase + NV_OFF_QT + swz128((2 * p + 1) * 8 + c, 16 * warp + 4 * h), wo);
+      }
+      // Scale bytes: [64 columns][16 blocks of 16 rows].
+#pragma unroll
+      for (int tq = 0; tq < 4; ++tq)
+        sts8(sbase + NV_OFF_TSC + (8 * c + 4 * mine + tq) * 16 + 2 * warp + (h >> 1), tcode[tq]);
+    }
+
+    // ---- barrier B: staging complete --------------------------------------
+    fence_proxy_async_smem();
+    bar_sync_nv();
+
+    if constexpr (COL) {
+      if (tid == 0) {
+        tma_store_3d(&tmap_qt, sbase + NV_OFF_QT, band * (NV_BAND / 2), tk * (NV_STEP_K / 8), 0);
+        bulk_commit();
+      }
+      // Transposed scale bytes: 16 per column per step; warp w takes 8 columns.
+      if (lane < NV_STEP_K / NV_WARPS) {
+        const int kc = warp * (NV_STEP_K / NV_WARPS) + lane;
+        const int k = tk * NV_STEP_K + kc;
+        const int mb0 = band * (NV_BAND / 16);
+        const int nvalid = min(NV_BAND / 16, nmb - mb0);
+        if (k < a.K) {
+          uint8_t* dst = a.s_t + static_cast<size_t>(k) * nmb + mb0;
+          const uint4 v = lds128(sbase + NV_OFF_TSC + kc * 16);
+          if (nvalid == 16 && (nmb & 15) == 0) {
+            stg128(dst, v.x, v.y, v.z, v.w);
           } else {
-            for (int bb = 0; bb < valid; ++bb) stg8(srow + bb, (w >> (8 * bb)) & 0xFFu);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            for (int bb = 0; bb < nvalid; ++bb) stg8(dst + bb, (wv[bb >> 2] >> (8 * (bb & 3))) & 0xFFu);
           }
         }
       }
     }
 
-    if constexpr (COL) {
-      uint8_t* qt = a.q_t + static_cast<size_t>(col0) * (a.M / 2) + row0 / 2;
-      const int nmb = a.M / 16;
-#pragma unroll
-      for (int jc = 0; jc < 8; ++jc) {
-        const uint32_t mag = (cm[jc >> 1] >> (16 * (jc & 1))) & 0xFFFFu;
-        uint32_t code;
-        float inv;
-        nv_block_scale(__uint_as_float(mag << 16), G, code, inv);
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          v[i] = ((jc & 1) ? bf16_hi(xr[i][jc >> 1]) : bf16_lo(xr[i][jc >> 1])) * inv;
-        const uint32_t w0 = cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
-        const uint32_t w1 = cvt_e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
-        if (col_ok && row_ok) {
-          stg64(qt + static_cast<size_t>(jc) * (a.M / 2), w0, w1);
-          stg8(a.s_t + static_cast<size_t>(col0 + jc) * nmb + row0 / 16, code);
+    if constexpr (ROW) {
+      // Rowwise codes: a group of four steps is one 256 x 128-byte TMA store;
+      // a partial group (range or band edge) is written by the threads.
+      const int slot4 = tk & 3;
+      if (rq_first < 0) rq_first = slot4;
+      const bool end = (tk + 1 == a.tiles_k) || (j + 1 == count);
+      if (slot4 == 3 || end) {
+        const int kbyte0 = (tk - slot4) * (NV_STEP_K / 2);   // first code byte of the group
+        if (rq_first == 0 && slot4 == 3) {
+          if (tid == 0) {
+            tma_store_3d(&tmap_qrow, sbase + NV_OFF_QR, kbyte0, band * (NV_BAND / 8), 0);
+            bulk_commit();
+          }
+        } else {
+          // thread tid writes row tid of the band, slots rq_first..slot4
+          const int row = band * NV_BAND + tid;
+          if (row < a.M) {
+            const int srow = (tid & 7) * 32 + (tid >> 3);
+            uint8_t* dst = a.q_row + static_cast<size_t>(row) * (a.K / 2) + kbyte0;
+            for (int sl = rq_first; sl <= slot4; ++sl) {
+              const int scol0 = (tk - slot4 + sl) * NV_STEP_K;   // first column of slot sl
+              for (int q4 = 0; q4 < 8 && scol0 + 8 * q4 < a.K; ++q4)
+                stg32(dst + sl * 32 + 4 * q4, lds32(sbase + NV_OFF_QR + swz128(srow, sl * 32 + 4 * q4)));
+            }
+          }
         }
+        rq_first = -1;
+      }
+      // Rowwise scale bytes: eight steps = one 32-byte sector per row.
+      const int slot8 = tk & 7;
+      if (rs_first < 0) rs_first = slot8;
+      if (slot8 == 7 || end) {
+        const int row = band * NV_BAND + tid;
+        if (row < a.M) {
+          const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
+          uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
+          const uint32_t src = sbase + NV_OFF_RSC + tid * 32;
+          if (rs_first == 0 && slot8 == 7 && (nkb & 7) == 0) {
+            const uint4 lo = lds128(src), hi = lds128(src + 16);
+            stg128(dst, lo.x, lo.y, lo.z, lo.w);
+            stg128(dst + 16, hi.x, hi.y, hi.z, hi.w);
+          } else {
+            const int b_end = min((slot8 + 1) * 4, nkb - kb0);
+            for (int bb = rs_first * 4; bb < b_end; ++bb)
+              stg8(dst + bb, (lds32(src + (bb & ~3)) >> (8 * (bb & 3))) & 0xFFu);
+          }
+        }
+        rs_first = -1;
       }
     }
-    __syncwarp();   // row_scale_stage is rewritten by the next tile
   }
+  if (tid == 0) bulk_wait_all();
 }
 
 // Largest |x| of a bf16 matrix.  Each block takes whole rows; 16-byte loads;
@@ -277,34 +467,35 @@ __global__ void selftest_wait_kernel(uint64_t timeout_ns, uint32_t* dev_err) {
 }
 
 template <int MODE>
-cudaError_t launch_nv_variant(const CUtensorMap& map, const NvArgs& a, int num_sms,
+cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms,
                               cudaStream_t stream) {
-  constexpr int SMEM = NV_WARPS * NV_STAGES * NV_TILE_M * NV_TILE_K * 2 + 128;
   auto kernel = nvfp4_quantize_kernel<MODE>;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (configured_device != dev) {
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, NV_SMEM);
     if (err != cudaSuccess) return err;
     configured_device = dev;
   }
-  const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
-  const int64_t ctas = (tiles + NV_WARPS - 1) / NV_WARPS;
-  const int grid = static_cast<int>(ctas < num_sms ? ctas : num_sms);
-  kernel<<<grid < 1 ? 1 : grid, NV_WARPS * 32, SMEM, stream>>>(map, a);
+  const int64_t steps = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
+  const int grid = static_cast<int>(steps < num_sms ? steps : num_sms);
+  kernel<<<grid < 1 ? 1 : grid, NV_WARPS * 32, NV_SMEM, stream>>>(maps.x, maps.q_row, maps.q_t, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_nvfp4(const CUtensorMap& map, const NvArgs& a, int mode, int num_sms,
+int nv_band_rows() { return NV_BAND; }
+int nv_step_cols() { return NV_STEP_K; }
+
+cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, int num_sms,
                          cudaStream_t stream) {
   switch (mode) {
-    case MX_ROW: return launch_nv_variant<MX_ROW>(map, a, num_sms, stream);
-    case MX_COL: return launch_nv_variant<MX_COL>(map, a, num_sms, stream);
-    default: return launch_nv_variant<MX_ROW | MX_COL>(map, a, num_sms, stream);
+    case MX_ROW: return launch_nv_variant<MX_ROW>(maps, a, num_sms, stream);
+    case MX_COL: return launch_nv_variant<MX_COL>(maps, a, num_sms, stream);
+    default: return launch_nv_variant<MX_ROW | MX_COL>(maps, a, num_sms, stream);
   }
 }
 

@@ -189,7 +189,9 @@ MXQ_API mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, f
  *   packed two per byte, element 2i in the low nibble.  A == 0 gives
  *   G = 0 and all-zero scales.
  *
- *   x       [M][ldx] bf16, M % 16 == 0, K % 16 == 0.
+ *   x       [M][ldx] bf16, M % 32 == 0, K % 32 == 0 (so that every packed
+ *           code row is a multiple of 16 bytes, as the bulk-copy engine
+ *           that writes them needs).
  *   flags   MXQ_ROWWISE and/or MXQ_COLWISE (= the transposed output).
  *   amax_in device fp32 tensor amax, or NULL to compute it here (then the
  *           workspace must hold 4 bytes).

@@ -76,6 +76,7 @@ def test_gated_and_nvfp4_host_validation():
     assert L.mx_quantize_gated(None, 64, 64, 128, 4, None, None, None, None, None, None) == 1
     nv = L.nvfp4_quantize_transpose
     assert nv(None, 24, 32, 32, 3, None, None, None, None, None, None, None, 0, None, None) == 2
+    assert nv(None, 48, 64, 64, 3, None, None, None, None, None, None, None, 0, None, None) == 2
     assert nv(None, 32, 32, 32, 0, None, None, None, None, None, None, None, 0, None, None) == 1
     assert nv(None, 32, 32, 32, 3, None, None, None, None, None, None, None, 0, None, None) == 1
     assert L.bf16_amax(None, 16, 12, 12, None, None) == 1

@@ -108,7 +108,8 @@ def test_mx_swiglu_row_only_and_col_only():
     check_activation_blocks(host(c["q_col"]), host(c["s_col"]), ref["q_col"], ref["s_col"], 1, "col")
 
 
-@pytest.mark.parametrize("M,K,seed", [(208, 176, 44), (16, 16, 45), (64, 64, 46), (512, 320, 47)])
+@pytest.mark.parametrize("M,K,seed", [(224, 160, 44), (32, 32, 45), (64, 64, 46), (512, 320, 47),
+                                      (768, 1600, 48)])
 @pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
 def test_nvfp4_bit_exact(M, K, seed, flags):
     bits = synth.nvfp4(M=M, K=K, seed=seed)
@@ -134,6 +135,31 @@ def test_nvfp4_given_amax_and_hand_block():
     for key in ("q_row", "s_row", "q_t", "s_t"):
         assert_equal_bytes(host(out[key]), ref[key], key)
     assert host(out["s_row"])[0, 0] == 0x38
+
+
+@pytest.mark.parametrize("amax_factor", [0.25, 1.0, 3.0])
+def test_nvfp4_caller_amax(amax_factor):
+    """A caller amax below the data's (block amaxes above it take the direct
+    scale computation), equal to it, and above it."""
+    bits = synth.nvfp4(M=256, K=512, seed=51)
+    A = np.float32(oracle.bf16_amax(bits) * amax_factor)
+    x = to_device(bits)
+    out = mxq.nvfp4_quantize_transpose(x, BOTH, amax=torch.tensor([A], device="cuda"))
+    ref = oracle.nvfp4_quantize(bits, tensor_amax=float(A))
+    assert host(out["global_scale"])[0] == np.float32(ref["global_scale"])
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        assert_equal_bytes(host(out[key]), ref[key], f"amax x{amax_factor} {key}")
+
+
+def test_nvfp4_wide_dynamic_range():
+    """Zero blocks, bf16 subnormal blocks and x1000 outliers: magnitudes far
+    below the scale table's 21 binades must still get code 0."""
+    bits = synth.dbias(M=512, K=256, seed=52)
+    x = to_device(bits)
+    out = mxq.nvfp4_quantize_transpose(x, BOTH)
+    ref = oracle.nvfp4_quantize(bits)
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        assert_equal_bytes(host(out[key]), ref[key], f"wide range {key}")
 
 
 def test_nvfp4_zero_tensor():
