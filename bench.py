@@ -67,17 +67,26 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha():
+# The sources each timed kernel is built from; a recorded DRAM traffic figure
+# counts only while these files are unchanged.
+KERNEL_SOURCES = {
+    "mx": ("mx_kernels.cu", "mxq_ptx.cuh", "mxq_internal.h"),
+    "nvfp4": ("nvfp4_kernels.cu", "mxq_ptx.cuh", "mxq_internal.h"),
+}
+
+
+def kernel_source_sha(family="mx"):
     h = hashlib.sha256()
-    for name in ("mx_kernels.cu", "mxq_ptx.cuh", "nvfp4_kernels.cu"):
+    for name in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "fp4_quantization_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+def recorded_traffic(kernel_key, family="mx"):
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/traffic.json), if it was taken on the current kernel sources;
+    else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -85,7 +94,7 @@ def recorded_traffic(kernel_key):
     except (OSError, ValueError):
         return None
     entry = rec.get(kernel_key)
-    if not entry or entry.get("source_sha") != kernel_source_sha():
+    if not entry or entry.get("source_sha") != kernel_source_sha(family):
         return None
     return entry.get("dram_bytes_per_launch")
 

@@ -11,10 +11,11 @@
 // the number of L2 write requests rather than by bytes: a 1-byte store costs
 // as much as a 32-byte one.  The kernel is laid out so every output leaves
 // in whole sectors or lines:
-//  * One CTA (BAND / 16 warps, one CTA per SM) walks a contiguous range of
-//    "steps"; a step is a band of BAND rows x 128 columns, loaded by one
-//    TMA box into a 2-slot ring (one mbarrier per slot).  Steps run along K
-//    inside a band, bands one after another.
+//  * One CTA of WARPS warps per SM (persistent) walks a contiguous range of
+//    "steps"; a step is a band of BAND = 16 * WARPS rows x 128 columns,
+//    loaded by one TMA box into a ring of STAGES slots (one mbarrier per
+//    slot).  Bands are taken GROUP at a time, and inside a group the steps
+//    run column by column with the group's bands interleaved.
 //  * Warp w owns rows 16w..16w+15 of the band; lane (h, c) = (lane / 16,
 //    lane % 16) owns rows 8h..8h+7 and columns 8c..8c+7 of those: 8
 //    conflict-free 16-byte shared loads (a quarter warp reads one contiguous
@@ -22,22 +23,23 @@
 //    xor-16 shuffle, then the two warps of a 32-row block swap their halves
 //    through shared memory at the step's first barrier; rowwise 1x32 amax:
 //    in-thread over 8 columns + xor-1 / xor-2 shuffles, two rows per
-//    register.  Small per-lane blocks keep registers at or below 128, so
-//    sixteen warps share an SM.
+//    register.
 //  * The shared scale is read off the exponent field of the amax; elements
 //    are multiplied by the exact power of two 2^-e (two per mul.rn.f32x2, no
 //    division; torchao PR #12, rationale) and converted two at a time by
 //    cvt.rn.satfinite.e4m3x2.f32.
 //  * Rowwise codes go straight to global memory: a half warp writes one full
 //    128-byte line per instruction.
-//  * Colwise codes of the whole band are staged in shared memory and leave
-//    through 3-D TMA stores over the [K][M] output viewed as
-//    [k % 8][k / 8][m] with 128-byte swizzle: every global segment is a full
-//    128-byte line, and the swizzle spreads one shared store instruction
-//    over all banks.
-//  * Rowwise scale bytes of 8 consecutive steps (1024 columns) are gathered
-//    in shared memory and written as one 32-byte sector per row; colwise
-//    scale bytes of a band (BAND / 32 blocks) leave as one run per column.
+//  * Colwise codes of the band are staged in shared memory and leave through
+//    3-D TMA stores over the [K][M] output viewed as [k % 8][k / 8][m] with
+//    128-byte swizzle: every global segment is a full 128-byte line, and the
+//    swizzle spreads one shared store instruction over all banks.  The
+//    group's bands follow one another along m, so a CTA writes GROUP * 128
+//    contiguous bytes of each colwise code row in consecutive steps.
+//  * Rowwise scale bytes of 8 consecutive column steps (1024 columns) are
+//    gathered in shared memory and written as one 32-byte sector per row;
+//    colwise scale bytes of the group's bands (GROUP * BAND / 32 blocks)
+//    leave as one run per column.
 //  * dbias: per step, the band's column sums are combined across warps in
 //    shared memory and written once per (band, column); a second small
 //    kernel adds the bands.
@@ -106,35 +108,48 @@ __device__ __forceinline__ void bar_sync_cta(int threads) {
 // Shared-memory layout of one CTA
 // ---------------------------------------------------------------------------
 
-template <int WARPS, int OPERANDS, int NSTAGES>
+template <int WARPS, int OPERANDS, int NSTAGES, int GROUP, int QBUF, int CPITCH>
 struct MxLayout {
   static constexpr int BAND = 16 * WARPS;
+  static constexpr int BPB = BAND / 32;                              // colwise blocks per band
   static constexpr int TILE_BYTES = BAND * MX_TILE_K * 2;            // one bf16 operand
   static constexpr int STAGE_BYTES = TILE_BYTES * OPERANDS;
   static constexpr int STAGES = NSTAGES;
   static constexpr int QCOL_HALF = 128 * MX_TILE_K;                  // 128 m x 128 k codes
   static constexpr int QCOL_HALVES = BAND / 128;
+  static constexpr int QCOL_BUF = QCOL_HALVES * QCOL_HALF;            // one step's codes
   static constexpr int OFF_QCOL = STAGES * STAGE_BYTES;              // 1024-aligned
-  static constexpr int OFF_RSC = OFF_QCOL + QCOL_HALVES * QCOL_HALF; // [BAND][8 slots][4]
-  static constexpr int OFF_CSC = OFF_RSC + BAND * 32;                // [128 cols][8 blocks]
-  static constexpr int OFF_DB = OFF_CSC + MX_TILE_K * 8;             // [WARPS][128] fp32
+  // [GROUP bands][BAND rows][8 steps][4 blocks]
+  static constexpr int OFF_RSC = OFF_QCOL + QBUF * QCOL_BUF;
+  // Colwise scale bytes, GROUP * BPB blocks of 128 columns: [128 columns]
+  // [CPITCH bytes] when there are four blocks (one 4-byte word per column),
+  // else [blocks][128 columns].
+  static constexpr bool CSC_BY_COL = GROUP * BPB == 4;
+  static_assert(CPITCH == 4 || CPITCH == 8, "column pitch of the scale staging");
+  static constexpr int OFF_CSC = OFF_RSC + GROUP * BAND * 32;
+  static constexpr int CSC_BYTES = CSC_BY_COL ? MX_TILE_K * CPITCH : GROUP * BPB * MX_TILE_K;
+  static constexpr int OFF_DB = OFF_CSC + CSC_BYTES;                 // [WARPS][128] fp32
   static constexpr int OFF_XCH = OFF_DB + WARPS * MX_TILE_K * 4;     // [WARPS][16][4] u32
   static constexpr int BYTES = OFF_XCH + WARPS * 16 * 16;
   static constexpr int DYNAMIC = BYTES + 1024;                       // + alignment pad
+  __device__ static constexpr int csc(int blk, int col) {
+    return CSC_BY_COL ? col * CPITCH + blk : blk * MX_TILE_K + col;
+  }
 };
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int MODE, bool DBIAS, int ACT, int WARPS, int STAGES>
+template <int MODE, bool DBIAS, int ACT, int WARPS, int STAGES, int GROUP, int QBUF,
+          int CPITCH>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_qcol, const MxArgs a) {
   constexpr bool ROW = (MODE & MX_ROW) != 0;
   constexpr bool COL = (MODE & MX_COL) != 0;
   constexpr int OPERANDS = (ACT == ACT_SWIGLU) ? 2 : 1;
-  using L = MxLayout<WARPS, OPERANDS, STAGES>;
+  using L = MxLayout<WARPS, OPERANDS, STAGES, GROUP, QBUF, CPITCH>;
   constexpr int THREADS = WARPS * 32;
   constexpr int BAND = L::BAND;
   constexpr int ROW_PITCH = MX_TILE_K * 2;   // bf16 tile row, bytes
@@ -153,24 +168,51 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int c = lane & 15;     // which 8-column chunk
   const uint32_t bar0 = smem_addr(&full_bar[0]);
 
-  // This CTA's contiguous range of steps; step t = band * tiles_k + tk.
+  // This CTA's contiguous range of steps.  Bands are taken GROUP at a time;
+  // inside a group the steps run column by column, the group's bands
+  // interleaved, so the colwise output of GROUP consecutive bands (and their
+  // colwise scale bytes) is written by one CTA in consecutive steps.
   const int64_t total = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
   const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
   const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
   const int count = t1 - t0;
   if (count <= 0) return;
 
-  auto issue_load = [&](int j) {   // thread 0 only
-    const int t = t0 + j;
-    const int band = t / a.tiles_k;
-    const int tk = t - band * a.tiles_k;
+  // Position of a step: group g (bands g * GROUP ..), its band count nb,
+  // band index bi inside the group and column step tk.  Decoded once for
+  // the range's first step, then advanced step by step.
+  struct Pos {
+    int g, nb, bi, tk;
+    __device__ int band() const { return g * GROUP + bi; }
+    __device__ void advance(int tiles_m, int tiles_k) {
+      if (++bi < nb) return;
+      bi = 0;
+      if (++tk < tiles_k) return;
+      tk = 0;
+      ++g;
+      nb = min(GROUP, tiles_m - g * GROUP);
+    }
+  };
+  Pos p0;
+  {
+    const int gsteps = GROUP * a.tiles_k;
+    p0.g = t0 / gsteps;
+    const int local = t0 - p0.g * gsteps;
+    p0.nb = min(GROUP, a.tiles_m - p0.g * GROUP);
+    p0.tk = local / p0.nb;
+    p0.bi = local - p0.tk * p0.nb;
+  }
+  Pos lpos = p0;   // next step to load (thread 0)
+
+  auto issue_load = [&](int j) {   // thread 0 only, for j = 0, 1, 2, ... in order
     const int s = j % STAGES;
     const uint32_t dst = sbase + s * L::STAGE_BYTES;
     mbar_arrive_expect_tx(bar0 + 8 * s, L::STAGE_BYTES);
-    tma_load_2d(dst, &tmap_x, tk * MX_TILE_K, band * BAND, bar0 + 8 * s);
+    tma_load_2d(dst, &tmap_x, lpos.tk * MX_TILE_K, lpos.band() * BAND, bar0 + 8 * s);
     if (OPERANDS == 2)
-      tma_load_2d(dst + L::TILE_BYTES, &tmap_x, a.up_col + tk * MX_TILE_K, band * BAND,
-                  bar0 + 8 * s);
+      tma_load_2d(dst + L::TILE_BYTES, &tmap_x, a.up_col + lpos.tk * MX_TILE_K,
+                  lpos.band() * BAND, bar0 + 8 * s);
+    lpos.advance(a.tiles_m, a.tiles_k);
   };
 
   if (tid == 0) {
@@ -185,13 +227,12 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
   const int nmb = a.M / 32;    // colwise scale bytes per column
   const int nkb = a.K / 32;    // rowwise scale bytes per row
-  int rsc_first = -1;          // first step slot gathered in the rowwise scale staging
 
-  for (int j = 0; j < count; ++j) {
+  Pos pos = p0;
+  for (int j = 0; j < count; ++j, pos.advance(a.tiles_m, a.tiles_k)) {
     const int s = j % STAGES;
-    const int t = t0 + j;
-    const int band = t / a.tiles_k;
-    const int tk = t - band * a.tiles_k;
+    const int band = pos.band();
+    const int tk = pos.tk;
     const bool ok = mbar_wait_bounded(bar0 + 8 * s, (j / STAGES) & 1, a.timeout_ns);
 
     const uint32_t my_row0 =
@@ -280,7 +321,7 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // staging is free (thread 0 waited for the previous store), the column
     // maxima are published, and every thread knows whether the copy landed.
     fence_proxy_async_smem();
-    if (COL && tid == 0) bulk_wait_read<0>();
+    if (COL && tid == 0) bulk_wait_read<QBUF - 1>();
     if (__syncthreads_or(!ok)) {
       // A copy never landed: record it, let the other copies in flight and
       // the pending stores finish (bounded), and stop without more output.
@@ -345,7 +386,8 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
       // Lane (h, c) holds block c/4's codes for its 8 rows; it stages rows
       // r and r + 4 (r = c & 3) into [BAND rows][8 slots][4 blocks].
       const int r = c & 3, b = c >> 2;
-      const uint32_t rs = sbase + L::OFF_RSC + (16 * warp + 8 * h + r) * 32 + slot * 4 + b;
+      const uint32_t rs =
+          sbase + L::OFF_RSC + (pos.bi * BAND + 16 * warp + 8 * h + r) * 32 + slot * 4 + b;
       const int sh = 16 * (r & 1);
       sts8(rs, ((r >> 1 ? rc[1] : rc[0]) >> sh) & 0xFFu);
       sts8(rs + 4 * 32, ((r >> 1 ? rc[3] : rc[2]) >> sh) & 0xFFu);
@@ -360,7 +402,8 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
       // [k % 8][k / 8][128 m], the 16-byte chunk index xor-ed with (k / 8) % 8
       // (the 128-byte swizzle of the store's tensor map).  The lane's 8 rows
       // are the h-th 8-byte half of chunk (warp % 8).
-      const uint32_t qs = sbase + L::OFF_QCOL + (warp >> 3) * L::QCOL_HALF + c * 128 +
+      const uint32_t qs = sbase + L::OFF_QCOL + (j % QBUF) * L::QCOL_BUF +
+                          (warp >> 3) * L::QCOL_HALF + c * 128 +
                           (((warp & 7) ^ (c & 7)) << 4) + 8 * h;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
@@ -377,15 +420,21 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         sts64(qs + (2 * p) * 2048, we[0] | (we[1] << 16), we[2] | (we[3] << 16));
         sts64(qs + (2 * p + 1) * 2048, wo[0] | (wo[1] << 16), wo[2] | (wo[3] << 16));
       }
-      // Scale bytes: [128 columns][BAND / 32 blocks]; both warps of a block
-      // hold the same codes, the even one writes them (h = 0: columns 0-3,
-      // h = 1: columns 4-7 of the lane's chunk).
+      // Scale bytes of block (band bi, warp / 2); both warps of a block hold
+      // the same codes, the even one writes them (h = 0: columns 0-3, h = 1:
+      // columns 4-7 of the lane's chunk).
       if ((warp & 1) == 0) {
+        const int blk = pos.bi * L::BPB + (warp >> 1);
+        if constexpr (L::CSC_BY_COL) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
-          sts8(sbase + L::OFF_CSC + (c * 8 + 4 * h + jj) * 8 + (warp >> 1),
-               (pair >> (16 * (jj & 1))) & 0xFFu);
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
+            sts8(sbase + L::OFF_CSC + L::csc(blk, c * 8 + 4 * h + jj),
+                 (pair >> (16 * (jj & 1))) & 0xFFu);
+          }
+        } else {
+          sts32(sbase + L::OFF_CSC + L::csc(blk, c * 8 + 4 * h),
+                h ? prmt(cc[2], cc[3], 0x6420) : prmt(cc[0], cc[1], 0x6420));
         }
       }
     }
@@ -420,47 +469,72 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
       if (tid == 0) {
 #pragma unroll
         for (int half = 0; half < L::QCOL_HALVES; ++half)
-          tma_store_3d(&tmap_qcol, sbase + L::OFF_QCOL + half * L::QCOL_HALF,
+          tma_store_3d(&tmap_qcol,
+                       sbase + L::OFF_QCOL + (j % QBUF) * L::QCOL_BUF + half * L::QCOL_HALF,
                        band * BAND + 128 * half, tk * (MX_TILE_K / 8), 0);
         bulk_commit();
       }
-      // Colwise scale bytes: one run of the band's blocks per column; every
-      // warp writes 128 / WARPS columns so no warp lengthens the step.
-      constexpr int COLS_PER_WARP = MX_TILE_K / WARPS;
-      if (lane < COLS_PER_WARP) {
-        const int kc = warp * COLS_PER_WARP + lane;
-        const int k = tk * MX_TILE_K + kc;
-        const int mb0 = band * (BAND / 32);
-        const int nvalid = min(BAND / 32, nmb - mb0);
-        if (k < a.K) {
-          uint8_t* dst = a.s_col + static_cast<size_t>(k) * nmb + mb0;
-          const uint32_t src = sbase + L::OFF_CSC + kc * 8;
-          const uint32_t lo = lds32(src), hi = lds32(src + 4);
-          if (BAND == 256 && nvalid == 8 && (nmb & 7) == 0) {
-            stg64(dst, lo, hi);
-          } else if (BAND == 128 && nvalid == 4 && (nmb & 3) == 0) {
-            stg32(dst, lo);
-          } else {
-            for (int bb = 0; bb < nvalid; ++bb)
-              stg8(dst + bb, ((bb < 4 ? lo : hi) >> (8 * (bb & 3))) & 0xFFu);
+      // Colwise scale bytes, once the group's last band (or this CTA's last
+      // step) is staged: one run of up to GROUP * BAND / 32 blocks per column.
+      if (pos.bi + 1 == pos.nb || j + 1 == count) {
+        constexpr int NB = GROUP * L::BPB;
+        constexpr int CH = NB < 16 ? NB : 16;               // bytes per store
+        const int fb = (pos.g == p0.g && tk == p0.tk) ? p0.bi : 0;   // first band staged
+        const int mb0 = (pos.g * GROUP + fb) * L::BPB;     // its first block along m
+        const int nblk = min((pos.bi + 1 - fb) * L::BPB, nmb - mb0);
+        if (nblk == NB && (nmb % CH) == 0) {
+          // Item i = (chunk, column); warp w takes items w * IPW .. + IPW - 1.
+          constexpr int ITEMS = MX_TILE_K * (NB / CH);
+          constexpr int IPW = ITEMS / WARPS;
+          static_assert(ITEMS % WARPS == 0 && IPW <= 32, "one item per lane");
+          if (lane < IPW) {
+            const int i = warp * IPW + lane;
+            const int kc = i % MX_TILE_K, ch = i / MX_TILE_K;
+            const int k = tk * MX_TILE_K + kc;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if constexpr (L::CSC_BY_COL) {
+              w[0] = lds32(sbase + L::OFF_CSC + L::csc(0, kc));
+            } else {
+#pragma unroll
+              for (int bb = 0; bb < CH; ++bb)
+                w[bb >> 2] |= ld_shared_u8(sbase + L::OFF_CSC + L::csc(ch * CH + bb, kc))
+                              << (8 * (bb & 3));
+            }
+            uint8_t* dst = a.s_col + static_cast<size_t>(k) * nmb + mb0 + ch * CH;
+            if (k < a.K) {
+              if (CH == 16) stg128(dst, w[0], w[1], w[2], w[3]);
+              else if (CH == 8) stg64(dst, w[0], w[1]);
+              else stg32(dst, w[0]);
+            }
+          }
+        } else {
+          for (int kc = tid; kc < MX_TILE_K; kc += THREADS) {
+            const int k = tk * MX_TILE_K + kc;
+            if (k >= a.K) continue;
+            uint8_t* dst = a.s_col + static_cast<size_t>(k) * nmb + mb0;
+            for (int bb = 0; bb < nblk; ++bb)
+              stg8(dst + bb, ld_shared_u8(sbase + L::OFF_CSC + L::csc(fb * L::BPB + bb, kc)));
           }
         }
       }
     }
 
     if constexpr (ROW) {
-      if (rsc_first < 0) rsc_first = slot;
-      const bool flush = (slot == 7) || (tk + 1 == a.tiles_k) || (j + 1 == count);
+      // This band's next step in this CTA, if any, is j + nb.
+      const bool flush = (slot == 7) || (tk + 1 == a.tiles_k) || (j + pos.nb >= count);
       if (flush) {
-        // Rowwise scale bytes of steps rsc_first..slot of this group of eight:
+        // Rowwise scale bytes of steps rsc_first..slot of this group of eight
+        // (the CTA's first step for this band may fall inside the group):
         // one 32-byte sector per row when all eight steps are present.  Warp
         // w writes the 16 rows it quantized.
+        const int first_tk = (pos.g == p0.g) ? p0.tk + (pos.bi < p0.bi ? 1 : 0) : 0;
+        const int rsc_first = first_tk > (tk & ~7) ? (first_tk & 7) : 0;
         const int rr = 16 * warp + lane;
         const int row = band * BAND + rr;
         if (lane < 16 && row < a.M) {
           const int kb0 = (tk - slot) * 4;   // first k-block of the group
           uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
-          const uint32_t src = sbase + L::OFF_RSC + rr * 32;
+          const uint32_t src = sbase + L::OFF_RSC + (pos.bi * BAND + rr) * 32;
           if (rsc_first == 0 && slot == 7 && (nkb & 7) == 0) {
             const uint4 lo = lds128(src), hi = lds128(src + 16);
             stg128(dst, lo.x, lo.y, lo.z, lo.w);
@@ -471,7 +545,6 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
               stg8(dst + bb, (lds32(src + (bb & ~3)) >> (8 * (bb & 3))) & 0xFFu);
           }
         }
-        rsc_first = -1;
       }
     }
 
@@ -532,20 +605,56 @@ __global__ void dbias_finalize_kernel(const float* __restrict__ ws, int bands, i
 #ifndef MXQ_SWIGLU_STAGES
 #define MXQ_SWIGLU_STAGES 2
 #endif
+#ifndef MXQ_PLAIN_GROUP
+#define MXQ_PLAIN_GROUP 1
+#endif
+#ifndef MXQ_PLAIN_GROUP_COL
+#define MXQ_PLAIN_GROUP_COL 8
+#endif
+#ifndef MXQ_PLAIN_QBUF
+#define MXQ_PLAIN_QBUF 1
+#endif
+#ifndef MXQ_GELU_GROUP
+#define MXQ_GELU_GROUP 1
+#endif
+#ifndef MXQ_GELU_GROUP_COL
+#define MXQ_GELU_GROUP_COL 8
+#endif
+#ifndef MXQ_GELU_QBUF
+#define MXQ_GELU_QBUF 1
+#endif
+#ifndef MXQ_SWIGLU_GROUP
+#define MXQ_SWIGLU_GROUP 1
+#endif
+#ifndef MXQ_SWIGLU_GROUP_COL
+#define MXQ_SWIGLU_GROUP_COL 8
+#endif
+#ifndef MXQ_SWIGLU_QBUF
+#define MXQ_SWIGLU_QBUF 1
+#endif
 template <int ACT>
 struct MxConfig {   // plain / dbias: band of 16 * WARPS rows
   static constexpr int WARPS = MXQ_PLAIN_WARPS;
   static constexpr int STAGES = MXQ_PLAIN_STAGES;
+  static constexpr int GROUP = MXQ_PLAIN_GROUP;          // with rowwise output
+  static constexpr int GROUP_COL = MXQ_PLAIN_GROUP_COL;  // colwise only
+  static constexpr int QBUF = MXQ_PLAIN_QBUF;            // colwise staging buffers
 };
 template <>
 struct MxConfig<ACT_GELU> {
   static constexpr int WARPS = MXQ_GELU_WARPS;
   static constexpr int STAGES = MXQ_GELU_STAGES;
+  static constexpr int GROUP = MXQ_GELU_GROUP;          // with rowwise output
+  static constexpr int GROUP_COL = MXQ_GELU_GROUP_COL;  // colwise only
+  static constexpr int QBUF = MXQ_GELU_QBUF;            // colwise staging buffers
 };
 template <>
 struct MxConfig<ACT_SWIGLU> {   // gate + up per slot
   static constexpr int WARPS = MXQ_SWIGLU_WARPS;
   static constexpr int STAGES = MXQ_SWIGLU_STAGES;
+  static constexpr int GROUP = MXQ_SWIGLU_GROUP;          // with rowwise output
+  static constexpr int GROUP_COL = MXQ_SWIGLU_GROUP_COL;  // colwise only
+  static constexpr int QBUF = MXQ_SWIGLU_QBUF;            // colwise staging buffers
 };
 
 template <int MODE, bool DBIAS, int ACT>
@@ -553,8 +662,16 @@ cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
                            cudaStream_t stream) {
   constexpr int WARPS = MxConfig<ACT>::WARPS;
   constexpr int STAGES = MxConfig<ACT>::STAGES;
-  using L = MxLayout<WARPS, ACT == ACT_SWIGLU ? 2 : 1, STAGES>;
-  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS, STAGES>;
+  // Rowwise code lines want each CTA to stay on one band along K; the
+  // colwise-only cast gains from interleaving bands (longer colwise runs).
+  constexpr int GROUP = (MODE & MX_ROW) ? MxConfig<ACT>::GROUP : MxConfig<ACT>::GROUP_COL;
+  constexpr int QBUF = MxConfig<ACT>::QBUF;
+  // Column pitch of the colwise scale staging (four blocks per column).  The
+  // pitch changes how the warps' store phases line up; measured on GB300,
+  // 8 bytes is faster for the plain cast and 4 bytes for the fused paths.
+  constexpr int CPITCH = (ACT == ACT_NONE && !DBIAS) ? 8 : 4;
+  using L = MxLayout<WARPS, ACT == ACT_SWIGLU ? 2 : 1, STAGES, GROUP, QBUF, CPITCH>;
+  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS, STAGES, GROUP, QBUF, CPITCH>;
 
   static int configured_device = -1;
   int dev = 0;

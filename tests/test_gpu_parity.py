@@ -43,6 +43,26 @@ def test_mx_rowcol_bit_exact(name, bits, _, flags):
         assert_equal_bytes(host(out[key]), ref[key], f"{name} {key}")
 
 
+@pytest.mark.parametrize("M,K,seed", [(3104, 2080, 48), (8192, 4096, 49)],
+                         ids=["ragged_groups", "whole_groups"])
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+def test_mx_rowcol_cta_ranges(M, K, seed, flags):
+    """Enough 128x128 steps that every SM walks a range of them: the first
+    shape has a ragged last band group and ragged K, with CTA ranges of two
+    or three steps that start and end inside band groups; the second gives
+    each CTA about thirteen steps, so some ranges cover whole groups and
+    their scale bytes leave in full runs."""
+    bits = synth.rowcol(M=M, K=K, seed=seed)
+    x = to_device(bits)
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mxq.mx_quantize_rowcol(x, flags, dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert dev_err.item() == 0
+    ref = oracle.mx_quantize(bits, flags)
+    for key in ref:
+        assert_equal_bytes(host(out[key]), ref[key], f"{M}x{K} {key}")
+
+
 def test_mx_rowcol_strided_input():
     """ldx > K: a column window of a wider matrix."""
     full = synth.rowcol(M=128, K=512, seed=35)
@@ -67,7 +87,8 @@ def _dbias_tolerance(bits):
     return 1e-5 * np.abs(xv).sum(axis=0) + 1e-30
 
 
-@pytest.mark.parametrize("M,K,seed", [(320, 224, 37), (32, 96, 38), (1024, 640, 39)])
+@pytest.mark.parametrize("M,K,seed", [(320, 224, 37), (32, 96, 38), (1024, 640, 39),
+                                      (3104, 2080, 50)])
 def test_mx_dbias(M, K, seed):
     bits = synth.dbias(M=M, K=K, seed=seed)
     x = to_device(bits)
@@ -79,8 +100,9 @@ def test_mx_dbias(M, K, seed):
     assert np.all(err <= _dbias_tolerance(bits)), f"dbias max err {err.max()}"
 
 
-def test_mx_gelu():
-    bits = synth.gelu(M=256, K=384, seed=40)
+@pytest.mark.parametrize("M,K,seed", [(256, 384, 40), (2080, 1184, 51)])
+def test_mx_gelu(M, K, seed):
+    bits = synth.gelu(M=M, K=K, seed=seed)
     x = to_device(bits)
     out = mxq.mx_quantize_rowcol(x, BOTH | mxq.ACT_GELU_TANH)
     ref = oracle.mx_quantize(bits, BOTH, act=oracle.ACT_GELU_TANH)
@@ -88,7 +110,7 @@ def test_mx_gelu():
     check_activation_blocks(host(out["q_col"]), host(out["s_col"]), ref["q_col"], ref["s_col"], 1, "gelu col")
 
 
-@pytest.mark.parametrize("M,N,seed", [(256, 352, 41), (64, 128, 42)])
+@pytest.mark.parametrize("M,N,seed", [(256, 352, 41), (64, 128, 42), (2080, 1184, 52)])
 def test_mx_swiglu(M, N, seed):
     bits = synth.swiglu(M=M, N=N, seed=seed)
     x = to_device(bits)
