@@ -297,6 +297,7 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
                                  "time includes it")
         if name.startswith("nvfp4_rowtrans_given"):
             out[name]["note"] = "tensor amax supplied by the caller: the quantize kernel alone"
+            out[name]["traffic"] = recorded_traffic("nvfp4_rowtrans_16384x8192", "nvfp4")
         del x, first, keep
         torch.cuda.empty_cache()
     return out
