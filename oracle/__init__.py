@@ -16,6 +16,7 @@ import numpy as np
 from . import build as _build
 
 ROWWISE, COLWISE, DBIAS = 1, 2, 4
+NVFP4_2D = 16
 ACT_NONE, ACT_GELU_TANH = 0, 1
 
 _lib = None
@@ -187,7 +188,8 @@ def bf16_amax(x):
 def nvfp4_quantize(x, tensor_amax=None, flags=ROWWISE | COLWISE):
     """NVFP4 quantize-transpose of bf16 bits x[M, K] given the tensor amax
     (computed over x when None).  Returns global_scale (float), q_row
-    [M,K/2], s_row [M,K/16], q_t [K,M/2], s_t [K,M/16]."""
+    [M,K/2], s_row [M,K/16], q_t [K,M/2], s_t [K,M/16].  flags | NVFP4_2D
+    takes one scale per 16x16 block."""
     p, M, K, ld = _matrix(x)
     if tensor_amax is None:
         tensor_amax = bf16_amax(x)

@@ -45,6 +45,10 @@
  *    the largest finite float if 1 / d overflows;
  *    every element becomes E2M1(x * inv), round-to-nearest-even, saturating
  *    to +-6;  A = 0 gives G = 0 and every scale 0.
+ *  The 2D variant (TE PR #3291, results table "NVFP4 2D quantize-transpose
+ *  kernel", fusion "nvfp42d") takes b over a 16x16 block instead, the rest
+ *  unchanged; its scale bytes keep the 1D layouts, each repeated over the
+ *  block's 16 rows (rowwise) or 16 columns (transposed).
  *
  *  NaN and infinite inputs are outside the contract; the choices made for
  *  them below are documented but not checked against the GPU.
@@ -320,14 +324,10 @@ float orc_bf16_amax(const uint16_t* x, int64_t M, int64_t K, int64_t ldx) {
     return amax;
 }
 
-/* One NVFP4 block of 16 values v[i * vs]; writes the E4M3 scale code and
- * the 16 E2M1 codes (one per byte, low nibble). */
-static void nvfp4_block(const float* v, int64_t vs, float G, uint8_t* scale, uint8_t* codes) {
-    float b = 0.0f;
-    for (int i = 0; i < 16; ++i) {
-        float a = fabsf(v[i * vs]);
-        if (a > b) b = a;
-    }
+/* The E4M3 scale code s of a block with amax b, and the reciprocal inv its
+ * elements are multiplied by (the recipe's steps 3-5, each one fp32
+ * operation). */
+static void nvfp4_scale(float b, float G, uint8_t* scale, float* inv_out) {
     uint8_t s = 0;
     float inv = 0.0f;
     if (G != 0.0f) {
@@ -340,10 +340,60 @@ static void nvfp4_block(const float* v, int64_t vs, float G, uint8_t* scale, uin
         }
     }
     *scale = s;
+    *inv_out = inv;
+}
+
+/* One NVFP4 block of 16 values v[i * vs]; writes the E4M3 scale code and
+ * the 16 E2M1 codes (one per byte, low nibble). */
+static void nvfp4_block(const float* v, int64_t vs, float G, uint8_t* scale, uint8_t* codes) {
+    float b = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        float a = fabsf(v[i * vs]);
+        if (a > b) b = a;
+    }
+    float inv;
+    nvfp4_scale(b, G, scale, &inv);
     for (int i = 0; i < 16; ++i) {
         float p = v[i * vs] * inv;
         codes[i] = orc_e2m1_encode((double)p);
     }
+}
+
+/* 2D variant: one scale per 16x16 block (rows 16 mb.., columns 16 kb..),
+ * from the amax of its 256 values; every element of the block is quantized
+ * with that scale in both outputs, and the scale byte is repeated in each of
+ * the block's 16 rows (rowwise scales) and 16 columns (transposed scales). */
+static void nvfp4_quantize_2d(const float* v, int64_t M, int64_t K, int flags, float G,
+                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_t, uint8_t* s_t) {
+    for (int64_t mb = 0; mb < M / 16; ++mb)
+        for (int64_t kb = 0; kb < K / 16; ++kb) {
+            float b = 0.0f;
+            for (int64_t i = 0; i < 16; ++i)
+                for (int64_t jj = 0; jj < 16; ++jj) {
+                    float a = fabsf(v[(mb * 16 + i) * K + kb * 16 + jj]);
+                    if (a > b) b = a;
+                }
+            uint8_t sc;
+            float inv;
+            nvfp4_scale(b, G, &sc, &inv);
+            for (int64_t i = 0; i < 16; ++i)
+                for (int64_t jj = 0; jj < 16; ++jj) {
+                    const int64_t m = mb * 16 + i, k = kb * 16 + jj;
+                    const uint8_t code = orc_e2m1_encode((double)(v[m * K + k] * inv));
+                    if (flags & ORC_ROWWISE) {
+                        uint8_t* byte = q_row + m * (K / 2) + k / 2;
+                        *byte = (k & 1) ? (uint8_t)((*byte & 0x0F) | (code << 4)) : code;
+                    }
+                    if (flags & ORC_COLWISE) {
+                        uint8_t* byte = q_t + k * (M / 2) + m / 2;
+                        *byte = (m & 1) ? (uint8_t)((*byte & 0x0F) | (code << 4)) : code;
+                    }
+                }
+            for (int64_t i = 0; i < 16; ++i) {
+                if (flags & ORC_ROWWISE) s_row[(mb * 16 + i) * (K / 16) + kb] = sc;
+                if (flags & ORC_COLWISE) s_t[(kb * 16 + i) * (M / 16) + mb] = sc;
+            }
+        }
 }
 
 int orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
@@ -359,6 +409,11 @@ int orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
     if (!v) return -1;
     for (int64_t m = 0; m < M; ++m)
         for (int64_t k = 0; k < K; ++k) v[m * K + k] = (float)orc_bf16_decode(x[m * ldx + k]);
+    if (flags & ORC_NVFP4_2D) {
+        nvfp4_quantize_2d(v, M, K, flags, G, q_row, s_row, q_t, s_t);
+        free(v);
+        return 0;
+    }
     uint8_t codes[16];
     if (flags & ORC_ROWWISE) {
         for (int64_t m = 0; m < M; ++m)

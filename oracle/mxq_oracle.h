@@ -33,7 +33,7 @@
 extern "C" {
 #endif
 
-enum { ORC_ROWWISE = 1, ORC_COLWISE = 2, ORC_DBIAS = 4 };
+enum { ORC_ROWWISE = 1, ORC_COLWISE = 2, ORC_DBIAS = 4, ORC_NVFP4_2D = 16 };
 enum { ORC_ACT_NONE = 0, ORC_ACT_GELU_TANH = 1 };
 
 /* Scalar format conversions. */
@@ -73,7 +73,10 @@ int orc_mx_quantize_swiglu(const uint16_t* x, int64_t M, int64_t N,
 float orc_bf16_amax(const uint16_t* x, int64_t M, int64_t K, int64_t ldx);
 
 /* NVFP4 quantize + transpose of x[M][K] given the tensor amax A.
- * flags: ORC_ROWWISE / ORC_COLWISE (the latter = transposed output). */
+ * flags: ORC_ROWWISE / ORC_COLWISE (the latter = transposed output);
+ * ORC_NVFP4_2D: one scale per 16x16 block instead of per 1x16 / 16x1 block
+ * (same output layouts, each block's scale repeated over its 16 rows or
+ * columns). */
 int orc_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                        float tensor_amax, int flags, float* global_scale,
                        uint8_t* q_row, uint8_t* s_row,

@@ -300,3 +300,86 @@ def test_nvfp4_transpose_symmetry_and_bound():
     in_range = np.abs(xv) <= 6.5 * d
     err = np.abs(xv - deq) - 0.5 * step - np.abs(xv) * 2.0 ** -22
     assert np.all(err[in_range] <= 0)
+
+
+# --------------------------------------------------------------------------
+# NVFP4 2D (16x16 blocks)
+# --------------------------------------------------------------------------
+
+TWO_D = oracle.NVFP4_2D
+
+
+def _unpack(q):
+    """Packed E2M1 bytes [R, C/2] -> codes [R, C] (element 2i in the low nibble)."""
+    return np.stack([q & 0xF, q >> 4], axis=2).reshape(q.shape[0], -1)
+
+
+def test_nvfp4_2d_hand_worked():
+    """Tensor amax 2688 makes G = 1.  Block (0, 0) has its amax 6 in row 0, so
+    every row of the block is scaled by s = 1.0 (0x38, inv 1): 0.5 in row 5
+    stays 0.5 (code 1), where a 1x16 block of that row alone (amax 0.5,
+    d = E4M3(0.5 / 6) = 0.0859375, 0.5 / d = 5.82 -> 6) gives it code 7.  Block (0, 1) is all zero;
+    block (1, 0) holds the tensor amax: s = 0x7E (448), inv = 1/448."""
+    x = np.zeros((32, 32), np.float32)
+    x[0, 0] = 6.0
+    x[5, 3] = 0.5
+    x[9, 15] = -1.5
+    x[15, 8] = 3.0
+    x[16, 0] = 2688.0
+    x[20, 4] = 896.0            # / 448 = 2 -> code 4
+    x[31, 15] = -0.0
+    out = oracle.nvfp4_quantize(bf16(x), tensor_amax=2688.0, flags=3 | TWO_D)
+    assert out["global_scale"] == 1.0
+    s_row, s_t = out["s_row"], out["s_t"]
+    assert np.all(s_row[:16, 0] == 0x38) and np.all(s_row[:16, 1] == 0)
+    assert np.all(s_row[16:, 0] == 0x7E) and np.all(s_row[16:, 1] == 0)
+    assert np.all(s_t[:16, 0] == 0x38) and np.all(s_t[:16, 1] == 0x7E)
+    assert np.all(s_t[16:, :] == 0)
+    c = _unpack(out["q_row"])
+    assert c[0, 0] == 0x7 and c[5, 3] == 0x1 and c[9, 15] == 0xB and c[15, 8] == 0x5
+    assert c[16, 0] == 0x7 and c[20, 4] == 0x4 and c[31, 15] == 0x8
+    assert np.count_nonzero(c) == 7
+    one_d = oracle.nvfp4_quantize(bf16(x), tensor_amax=2688.0, flags=oracle.ROWWISE)
+    assert _unpack(one_d["q_row"])[5, 3] == 0x7        # the 1x16 reading differs
+
+
+def test_nvfp4_2d_transposed_output_is_the_transpose():
+    """Each element takes its block's scale in both outputs, so the
+    transposed codes are the rowwise codes transposed, and the transposed
+    scale of (k, block mb) is the rowwise scale of (rows of mb, k / 16)."""
+    x = synth.nvfp4(M=96, K=160, seed=13)
+    out = oracle.nvfp4_quantize(x, flags=3 | TWO_D)
+    np.testing.assert_array_equal(_unpack(out["q_t"]), _unpack(out["q_row"]).T)
+    per_block = out["s_row"][::16, :]                       # [M/16, K/16]
+    np.testing.assert_array_equal(out["s_row"], np.repeat(per_block, 16, axis=0))
+    np.testing.assert_array_equal(out["s_t"], np.repeat(per_block.T, 16, axis=0))
+
+
+def test_nvfp4_2d_transpose_symmetry():
+    """The 2D blocks of x^T are the transposed blocks of x."""
+    x = synth.nvfp4(M=64, K=96, seed=14)
+    a = oracle.nvfp4_quantize(x, flags=3 | TWO_D)
+    b = oracle.nvfp4_quantize(np.ascontiguousarray(x.T), tensor_amax=oracle.bf16_amax(x),
+                              flags=3 | TWO_D)
+    np.testing.assert_array_equal(a["q_t"], b["q_row"])
+    np.testing.assert_array_equal(a["s_t"], b["s_row"])
+    np.testing.assert_array_equal(a["q_row"], b["q_t"])
+
+
+def test_nvfp4_2d_reduces_to_1d_on_repeated_rows_and_columns():
+    """When the 16 rows of every block are equal, a 16x16 block has the amax
+    of each of its 1x16 rows, so the 2D rowwise output equals the 1D one;
+    likewise for the transposed output when the 16 columns are equal."""
+    base = synth.nvfp4(M=64, K=128, seed=15)
+    rows = np.repeat(base[::16], 16, axis=0)               # rows repeat in 16-row groups
+    A = oracle.bf16_amax(rows)
+    two = oracle.nvfp4_quantize(rows, tensor_amax=A, flags=3 | TWO_D)
+    one = oracle.nvfp4_quantize(rows, tensor_amax=A, flags=3)
+    np.testing.assert_array_equal(two["q_row"], one["q_row"])
+    np.testing.assert_array_equal(two["s_row"], one["s_row"])
+    cols = np.repeat(base[:, ::16], 16, axis=1)            # columns repeat in 16-column groups
+    A = oracle.bf16_amax(cols)
+    two = oracle.nvfp4_quantize(cols, tensor_amax=A, flags=3 | TWO_D)
+    one = oracle.nvfp4_quantize(cols, tensor_amax=A, flags=3)
+    np.testing.assert_array_equal(two["q_t"], one["q_t"])
+    np.testing.assert_array_equal(two["s_t"], one["s_t"])
