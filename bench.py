@@ -265,6 +265,14 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
         ("nvfp4_rowtrans_given_amax_16384x8192", lambda: synth.nvfp4(),
          lambda x, o: mxq.nvfp4_quantize_transpose(x, mxq.ROWWISE | mxq.COLWISE, **o),
          nvfp4_bytes(16384, 8192), {}),
+        ("nvfp4_2d_rowtrans_given_amax_16384x8192", lambda: synth.nvfp4(),
+         lambda x, o: mxq.nvfp4_quantize_transpose(x, mxq.ROWWISE | mxq.COLWISE | mxq.NVFP4_2D,
+                                                   **o),
+         nvfp4_bytes(16384, 8192), {}),
+        ("nvfp4_2d_rowtrans_given_amax_8192x8192", lambda: synth.nvfp4(M=8192, K=8192),
+         lambda x, o: mxq.nvfp4_quantize_transpose(x, mxq.ROWWISE | mxq.COLWISE | mxq.NVFP4_2D,
+                                                   **o),
+         nvfp4_bytes(8192, 8192), {}),
         ("bf16_amax_16384x8192", lambda: synth.nvfp4(),
          lambda x, o: mxq.bf16_amax(x, **o), 16384 * 8192 * 2 + 4, {}),
     ]
@@ -277,7 +285,7 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
             keep = {"out": first}
         else:
             keep = dict(first)
-        if name.startswith("nvfp4_rowtrans_given_amax"):
+        if "given_amax" in name:
             keep["amax"] = mxq.bf16_amax(x)
         elif name.startswith("nvfp4"):
             keep["workspace"] = torch.empty(16, dtype=torch.uint8, device=device)
@@ -295,9 +303,10 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
         if name.startswith("nvfp4_rowtrans_16"):
             out[name]["note"] = ("bytes exclude the tensor-amax pass (a second 256 MiB read), "
                                  "time includes it")
-        if name.startswith("nvfp4_rowtrans_given"):
+        if "given_amax" in name:
             out[name]["note"] = "tensor amax supplied by the caller: the quantize kernel alone"
-            out[name]["traffic"] = recorded_traffic("nvfp4_rowtrans_16384x8192", "nvfp4")
+            if name == "nvfp4_rowtrans_given_amax_16384x8192":
+                out[name]["traffic"] = recorded_traffic("nvfp4_rowtrans_16384x8192", "nvfp4")
         del x, first, keep
         torch.cuda.empty_cache()
     return out

@@ -18,6 +18,7 @@ ROWWISE = 1
 COLWISE = 2
 DBIAS = 4
 ACT_GELU_TANH = 8
+NVFP4_2D = 16
 OP_ROWCOL = 0
 OP_NVFP4 = 1
 DEVERR_TIMEOUT = 1
@@ -166,7 +167,8 @@ def nvfp4_quantize_transpose(x, flags=ROWWISE | COLWISE, *, amax=None, global_sc
                              dev_err=None, stream=None):
     """bf16 x[M, K] -> NVFP4: q_row [M,K/2] / s_row [M,K/16] (ROWWISE),
     q_t [K,M/2] / s_t [K,M/16] (COLWISE), global_scale [1] fp32.  `amax`
-    (1-element fp32 device tensor) skips the internal amax pass."""
+    (1-element fp32 device tensor) skips the internal amax pass; flags | NVFP4_2D
+    takes one scale per 16x16 block."""
     ldx = _input(x)
     M, K = x.shape
     dev = x.device

@@ -288,7 +288,7 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
                                     uint8_t* q_row, uint8_t* s_row, uint8_t* q_t, uint8_t* s_t,
                                     void* workspace, size_t workspace_bytes, uint32_t* dev_err,
                                     mxq_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE)) return MXQ_EINVAL;
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_NVFP4_2D)) return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if (M < 0 || K < 0 || ldx < K) return MXQ_ESHAPE;
   if ((M % 32) || (K % 32)) return MXQ_ESHAPE;
@@ -342,7 +342,8 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   if (st != MXQ_OK) return st;
   st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t);
   if (st != MXQ_OK) return st;
-  return from_cuda(mxq::launch_nvfp4(maps, a, direction_mode(flags), sms, stream));
+  return from_cuda(mxq::launch_nvfp4(maps, a, direction_mode(flags), (flags & MXQ_NVFP4_2D) != 0,
+                                     sms, stream));
 }
 
 mxq_status mxq_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* dev_err, mxq_stream_t stream) {

@@ -5,7 +5,8 @@
 // of TE PR #3291 "Fix pointer arithmatic to generate correct LDS/STS
 // instructions" (results table "NVFP4 2D quantize-transpose kernel" and the
 // 1D kernel named in its "Patched but not measurable" section); this file
-// implements the 1D (1x16 block) variant.
+// implements both: 1D (1x16 rowwise / 16x1 transposed blocks) and 2D (one
+// scale per 16x16 block, used by both outputs).
 //
 // Layout of the work (same principles as the MXFP8 kernel: every output
 // leaves in whole lines or sectors, because the write side costs by L2
@@ -18,7 +19,9 @@
 //    16-byte shared loads).  A 1x16 row block spans lanes c = 2b, 2b+1 and a
 //    16x1 transposed block spans lanes h = 2g, 2g+1: one xor shuffle each.
 //  * Each block scale is computed once: the two lanes of a pair split the
-//    rows (or columns) and swap the reciprocals with one shuffle.  The scale
+//    rows (or columns) and swap the reciprocals with one shuffle.  A 16x16
+//    block spans the four lanes (h pair) x (c pair): its amax takes the
+//    xor-1 and xor-8 shuffles and every lane looks its one scale up.  The scale
 //    arithmetic is IEEE fp32 with explicit rounding intrinsics in the fixed
 //    order (b / 6) / G -> E4M3 -> value * G -> 1 / d; each element then
 //    takes one multiply by that reciprocal (two per mul.rn.f32x2; no
@@ -119,7 +122,7 @@ __device__ __forceinline__ uint32_t swz128(int row, int byte) {
   return row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
 }
 
-template <int MODE>
+template <int MODE, bool TWO_D>
 __global__ void __launch_bounds__(NV_WARPS * 32, 1)
 nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                       const __grid_constant__ CUtensorMap tmap_qrow,
@@ -247,6 +250,17 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const bool col_ok = col0 < a.K;
     const bool row_ok = row0 < a.M;
 
+    // 2D: the 16x16 block's amax over the four lanes that hold it, and its
+    // one scale.
+    uint32_t code2d = 0u;
+    float inv2d = 0.0f;
+    if constexpr (TWO_D) {
+      uint32_t m2 = absmax_bf16x2(absmax_bf16x2(rm[0], rm[1]), absmax_bf16x2(rm[2], rm[3]));
+      m2 = absmax_bf16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
+      m2 = absmax_bf16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 8));
+      tabs.lookup(max(mag16(m2, 0), mag16(m2, 1)), code2d, inv2d);
+    }
+
     // The lane's values widened to fp32 once, for both directions.
     float2 xv[8][4];
 #pragma unroll
@@ -257,23 +271,32 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
     // ---- rowwise: block scales (split over the c pair), codes, scale bytes --
     if constexpr (ROW) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) rm[q] = absmax_bf16x2(rm[q], __shfl_xor_sync(0xFFFFFFFFu, rm[q], 1));
       const int mine = c & 1;               // this lane scales rows 4*mine .. 4*mine+3
       uint32_t rcode[4];
-      float rinv_own[4], rinv_oth[4];
-#pragma unroll
-      for (int tq = 0; tq < 4; ++tq) {
-        const uint32_t pair = mine ? rm[2 + (tq >> 1)] : rm[tq >> 1];
-        tabs.lookup(mag16(pair, tq & 1), rcode[tq], rinv_own[tq]);
-      }
-#pragma unroll
-      for (int tq = 0; tq < 4; ++tq) rinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, rinv_own[tq], 1);
       float rinv[8];
+      if constexpr (TWO_D) {
 #pragma unroll
-      for (int tq = 0; tq < 4; ++tq) {
-        rinv[tq] = mine ? rinv_oth[tq] : rinv_own[tq];
-        rinv[4 + tq] = mine ? rinv_own[tq] : rinv_oth[tq];
+        for (int tq = 0; tq < 4; ++tq) rcode[tq] = code2d;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rinv[i] = inv2d;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          rm[q] = absmax_bf16x2(rm[q], __shfl_xor_sync(0xFFFFFFFFu, rm[q], 1));
+        float rinv_own[4], rinv_oth[4];
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) {
+          const uint32_t pair = mine ? rm[2 + (tq >> 1)] : rm[tq >> 1];
+          tabs.lookup(mag16(pair, tq & 1), rcode[tq], rinv_own[tq]);
+        }
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq)
+          rinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, rinv_own[tq], 1);
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) {
+          rinv[tq] = mine ? rinv_oth[tq] : rinv_own[tq];
+          rinv[4 + tq] = mine ? rinv_own[tq] : rinv_oth[tq];
+        }
       }
       // Codes of row i: 8 values -> 4 bytes at k / 2 = 4c within this step.
       const int slot4 = tk & 3;
@@ -299,23 +322,32 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
     // ---- transposed: block scales (split over the h pair), codes, scales ----
     if constexpr (COL) {
-#pragma unroll
-      for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], __shfl_xor_sync(0xFFFFFFFFu, cm[p], 8));
       const int mine = h & 1;               // this lane scales columns 4*mine .. 4*mine+3
       uint32_t tcode[4];
-      float tinv_own[4], tinv_oth[4];
-#pragma unroll
-      for (int tq = 0; tq < 4; ++tq) {
-        const uint32_t pair = mine ? cm[2 + (tq >> 1)] : cm[tq >> 1];
-        tabs.lookup(mag16(pair, tq & 1), tcode[tq], tinv_own[tq]);
-      }
-#pragma unroll
-      for (int tq = 0; tq < 4; ++tq) tinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, tinv_own[tq], 8);
       float tinv[8];
+      if constexpr (TWO_D) {
 #pragma unroll
-      for (int tq = 0; tq < 4; ++tq) {
-        tinv[tq] = mine ? tinv_oth[tq] : tinv_own[tq];
-        tinv[4 + tq] = mine ? tinv_own[tq] : tinv_oth[tq];
+        for (int tq = 0; tq < 4; ++tq) tcode[tq] = code2d;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tinv[i] = inv2d;
+      } else {
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          cm[p] = absmax_bf16x2(cm[p], __shfl_xor_sync(0xFFFFFFFFu, cm[p], 8));
+        float tinv_own[4], tinv_oth[4];
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) {
+          const uint32_t pair = mine ? cm[2 + (tq >> 1)] : cm[tq >> 1];
+          tabs.lookup(mag16(pair, tq & 1), tcode[tq], tinv_own[tq]);
+        }
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq)
+          tinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, tinv_own[tq], 8);
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) {
+          tinv[tq] = mine ? tinv_oth[tq] : tinv_own[tq];
+          tinv[4 + tq] = mine ? tinv_own[tq] : tinv_oth[tq];
+        }
       }
       // Codes of column jc: 8 rows -> 4 bytes at m / 2 = 16 * warp + 4h.
 #pragma unroll
@@ -466,10 +498,10 @@ __global__ void selftest_wait_kernel(uint64_t timeout_ns, uint32_t* dev_err) {
   if (__any_sync(0xFFFFFFFFu, !ok) && threadIdx.x == 0) atomicOr(dev_err, 1u);
 }
 
-template <int MODE>
+template <int MODE, bool TWO_D>
 cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms,
                               cudaStream_t stream) {
-  auto kernel = nvfp4_quantize_kernel<MODE>;
+  auto kernel = nvfp4_quantize_kernel<MODE, TWO_D>;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -485,18 +517,25 @@ cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms,
   return cudaGetLastError();
 }
 
+template <bool TWO_D>
+cudaError_t launch_nv_mode(const NvMaps& maps, const NvArgs& a, int mode, int num_sms,
+                           cudaStream_t stream) {
+  switch (mode) {
+    case MX_ROW: return launch_nv_variant<MX_ROW, TWO_D>(maps, a, num_sms, stream);
+    case MX_COL: return launch_nv_variant<MX_COL, TWO_D>(maps, a, num_sms, stream);
+    default: return launch_nv_variant<MX_ROW | MX_COL, TWO_D>(maps, a, num_sms, stream);
+  }
+}
+
 }  // namespace
 
 int nv_band_rows() { return NV_BAND; }
 int nv_step_cols() { return NV_STEP_K; }
 
-cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, int num_sms,
-                         cudaStream_t stream) {
-  switch (mode) {
-    case MX_ROW: return launch_nv_variant<MX_ROW>(maps, a, num_sms, stream);
-    case MX_COL: return launch_nv_variant<MX_COL>(maps, a, num_sms, stream);
-    default: return launch_nv_variant<MX_ROW | MX_COL>(maps, a, num_sms, stream);
-  }
+cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two_d,
+                         int num_sms, cudaStream_t stream) {
+  return two_d ? launch_nv_mode<true>(maps, a, mode, num_sms, stream)
+               : launch_nv_mode<false>(maps, a, mode, num_sms, stream);
 }
 
 cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,

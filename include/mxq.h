@@ -70,7 +70,8 @@ enum {
     MXQ_COLWISE = 2,        /* 32x1 (MX) / 16x1 (NVFP4) blocks along M,    */
                             /* stored transposed: [K][M]                   */
     MXQ_DBIAS = 4,          /* fp32 column sums of x (mx_quantize_rowcol)  */
-    MXQ_ACT_GELU_TANH = 8   /* quantize gelu_tanh(x) (mx_quantize_rowcol)  */
+    MXQ_ACT_GELU_TANH = 8,  /* quantize gelu_tanh(x) (mx_quantize_rowcol)  */
+    MXQ_NVFP4_2D = 16       /* 16x16 blocks (nvfp4_quantize_transpose)     */
 };
 
 /* bits of *dev_err */
@@ -177,8 +178,10 @@ MXQ_API mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, f
 /*
  * nvfp4_quantize_transpose -- bf16 -> NVFP4, rowwise and transposed.
  *
- * Operation (TE PR #3291, "NVFP4 quantize-transpose" family, 1D variant;
- * every step one fp32 IEEE operation in this order):
+ * Operation (TE PR #3291, "NVFP4 quantize-transpose" family: the 1D kernel
+ * named in "Patched but not measurable" and the results table "NVFP4 2D
+ * quantize-transpose kernel"; every step one fp32 IEEE operation in this
+ * order):
  *   A = tensor amax (from amax_in, else from an internal bf16_amax pass);
  *   G = A / 2688 (2688 = 448 * 6), written to *global_scale;
  *   per block of 16 values (1x16 along K rowwise; 16x1 along M for the
@@ -188,11 +191,17 @@ MXQ_API mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, f
  *   codes = E2M1(x * inv), round-to-nearest-even, saturating to +-6,
  *   packed two per byte, element 2i in the low nibble.  A == 0 gives
  *   G = 0 and all-zero scales.
+ *   With MXQ_NVFP4_2D the block is 16x16 (rows 16i.., columns 16j..): b is
+ *   its amax and every element of it is quantized with its one scale in
+ *   both outputs; the scale arrays keep the shapes below, each block's
+ *   scale repeated in its 16 rows (s_row) or 16 columns (s_t), so q_t is
+ *   exactly the transpose of q_row.
  *
  *   x       [M][ldx] bf16, M % 32 == 0, K % 32 == 0 (so that every packed
  *           code row is a multiple of 16 bytes, as the bulk-copy engine
  *           that writes them needs).
- *   flags   MXQ_ROWWISE and/or MXQ_COLWISE (= the transposed output).
+ *   flags   MXQ_ROWWISE and/or MXQ_COLWISE (= the transposed output),
+ *           optional MXQ_NVFP4_2D.
  *   amax_in device fp32 tensor amax, or NULL to compute it here (then the
  *           workspace must hold 4 bytes).
  *   global_scale  device fp32, receives G (required).

@@ -132,3 +132,22 @@ def test_nvfp4_16384x8192():
                            f"nvfp4 q_t ({m0},{k0})")
         assert_equal_bytes(host(out["s_t"][k0:k0 + 128, m0 // 16:(m0 + 64) // 16]), ref["s_t"],
                            f"nvfp4 s_t ({m0},{k0})")
+
+
+def test_nvfp4_2d_16384x8192():
+    """16x16 blocks at the NVFP4 workload size, windows aligned to blocks."""
+    bits = synth.nvfp4()
+    x = to_device(bits)
+    out = mxq.nvfp4_quantize_transpose(x, BOTH | mxq.NVFP4_2D)
+    A = oracle.bf16_amax(bits)
+    for m0, k0 in windows(16384, 8192, 64, 128, 40, seed=7, align=16):
+        ref = oracle.nvfp4_quantize(bits[m0:m0 + 64, k0:k0 + 128], tensor_amax=A,
+                                    flags=BOTH | oracle.NVFP4_2D)
+        assert_equal_bytes(host(out["q_row"][m0:m0 + 64, k0 // 2:(k0 + 128) // 2]), ref["q_row"],
+                           f"2d q_row ({m0},{k0})")
+        assert_equal_bytes(host(out["s_row"][m0:m0 + 64, k0 // 16:(k0 + 128) // 16]), ref["s_row"],
+                           f"2d s_row ({m0},{k0})")
+        assert_equal_bytes(host(out["q_t"][k0:k0 + 128, m0 // 2:(m0 + 64) // 2]), ref["q_t"],
+                           f"2d q_t ({m0},{k0})")
+        assert_equal_bytes(host(out["s_t"][k0:k0 + 128, m0 // 16:(m0 + 64) // 16]), ref["s_t"],
+                           f"2d s_t ({m0},{k0})")

@@ -194,6 +194,35 @@ def test_nvfp4_zero_tensor():
         assert_equal_bytes(host(out[key]), ref[key], key)
 
 
+@pytest.mark.parametrize("M,K,seed", [(224, 160, 53), (32, 32, 54), (512, 320, 55),
+                                      (768, 1600, 56), (3104, 2080, 57)])
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+def test_nvfp4_2d_bit_exact(M, K, seed, flags):
+    """16x16 blocks: several CTA steps, ragged bands and ranges."""
+    bits = synth.nvfp4(M=M, K=K, seed=seed)
+    x = to_device(bits)
+    out = mxq.nvfp4_quantize_transpose(x, flags | mxq.NVFP4_2D)
+    ref = oracle.nvfp4_quantize(bits, flags=flags | oracle.NVFP4_2D)
+    assert host(out["global_scale"])[0] == np.float32(ref["global_scale"])
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        if key in ref:
+            assert_equal_bytes(host(out[key]), ref[key], f"nvfp4 2d {key}")
+
+
+@pytest.mark.parametrize("amax_factor", [0.25, 1.0, 3.0])
+def test_nvfp4_2d_caller_amax_and_wide_range(amax_factor):
+    """Caller amax below, at and above the data's, on an input with zero and
+    subnormal blocks and outliers."""
+    bits = synth.dbias(M=256, K=512, seed=58)
+    A = np.float32(oracle.bf16_amax(bits) * amax_factor)
+    x = to_device(bits)
+    out = mxq.nvfp4_quantize_transpose(x, BOTH | mxq.NVFP4_2D,
+                                       amax=torch.tensor([A], device="cuda"))
+    ref = oracle.nvfp4_quantize(bits, tensor_amax=float(A), flags=BOTH | oracle.NVFP4_2D)
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        assert_equal_bytes(host(out[key]), ref[key], f"2d amax x{amax_factor} {key}")
+
+
 @pytest.mark.parametrize("M,K", [(96, 256), (1, 8), (333, 72)])
 def test_bf16_amax(M, K):
     bits = synth.nvfp4(M=max(M, 16), K=max(K, 16), seed=48)[:M, :K].copy()
