@@ -45,15 +45,28 @@
 namespace mxq {
 namespace {
 
+#ifndef MXQ_NV_STAGES
+#define MXQ_NV_STAGES 3
+#endif
+#ifndef MXQ_NV_LOAD_HINT
+#define MXQ_NV_LOAD_HINT 1
+#endif
+
 constexpr int NV_WARPS = 8;
-constexpr int NV_STAGES = 3;
+constexpr int NV_STAGES = MXQ_NV_STAGES;
 constexpr int NV_BAND = 32 * NV_WARPS;            // 256 rows per step
 constexpr int NV_STEP_K = 64;                     // columns per step
 constexpr int NV_STAGE_BYTES = NV_BAND * NV_STEP_K * 2;          // 32 KiB
 constexpr int NV_OFF_QT = NV_STAGES * NV_STAGE_BYTES;            // [8][8][128 B]
 constexpr int NV_OFF_QR = NV_OFF_QT + NV_STEP_K * NV_BAND / 2;   // [8][32][128 B]
-constexpr int NV_OFF_RSC = NV_OFF_QR + NV_BAND * 128;            // [256 rows][8 slots][4]
-constexpr int NV_OFF_TSC = NV_OFF_RSC + NV_BAND * 32;            // [64 cols][16 blocks]
+// Rowwise scale bytes [256 rows][8 slots][4 blocks], rows 36 bytes apart so
+// that consecutive rows fall in different banks.
+constexpr int NV_RSC_PITCH = 36;
+constexpr int NV_OFF_RSC = NV_OFF_QR + NV_BAND * 128;
+// Transposed scale bytes [64 cols][16 blocks]; the four 4-byte words of
+// column k are rotated by (k / 8) % 4 so that the lanes storing the columns
+// 8 apart use different banks.
+constexpr int NV_OFF_TSC = NV_OFF_RSC + NV_BAND * NV_RSC_PITCH;
 constexpr int NV_OFF_INV = NV_OFF_TSC + NV_STEP_K * 16;          // [128] fp32 1/d per code
 constexpr int NV_TAB_BINADES = 21;                               // code table: binades kept
 constexpr int NV_OFF_CODE = NV_OFF_INV + 128 * 4;                // [21 x 128] E4M3 codes
@@ -122,6 +135,15 @@ __device__ __forceinline__ uint32_t swz128(int row, int byte) {
   return row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
 }
 
+// Byte offset of block `blk` of column `col` in the transposed scale staging.
+__device__ __forceinline__ uint32_t tsc_offset(int col, int blk) {
+  return col * 16 + ((((blk >> 2) + (col >> 3)) & 3) << 2) + (blk & 3);
+}
+
+__device__ __forceinline__ uint32_t pick4(const uint32_t v[4], int i) {
+  return (i & 2) ? ((i & 1) ? v[3] : v[2]) : ((i & 1) ? v[1] : v[0]);
+}
+
 template <int MODE, bool TWO_D>
 __global__ void __launch_bounds__(NV_WARPS * 32, 1)
 nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -180,7 +202,12 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int tk = t - band * a.tiles_k;
     const int s = j % NV_STAGES;
     mbar_arrive_expect_tx(bar0 + 8 * s, NV_STAGE_BYTES);
+#if MXQ_NV_LOAD_HINT
+    tma_load_2d_hint(sbase + s * NV_STAGE_BYTES, &tmap_x, tk * NV_STEP_K, band * NV_BAND,
+                     bar0 + 8 * s, l2_policy_evict_last());
+#else
     tma_load_2d(sbase + s * NV_STAGE_BYTES, &tmap_x, tk * NV_STEP_K, band * NV_BAND, bar0 + 8 * s);
+#endif
   };
 
   if (tid == 0) {
@@ -312,12 +339,22 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const int srow = i * 32 + 4 * warp + h;
         sts32(sbase + NV_OFF_QR + swz128(srow, slot4 * 32 + 4 * c), w);
       }
-      // Scale bytes: [256 rows][8 slots][4 blocks of 16 columns].
+      // Scale bytes: [256 rows][8 slots][4 blocks of 16 columns].  The four
+      // lanes c = mine, mine + 2, mine + 4, mine + 6 hold blocks 0..3 of the
+      // same four rows; lane b = c / 2 gathers row 4 * mine + b from the
+      // other three (three shuffles) and stores one 4-byte word.
       const int slot8 = tk & 7;
+      const int b = c >> 1;
+      uint32_t word = pick4(rcode, b) << (8 * b);
 #pragma unroll
-      for (int tq = 0; tq < 4; ++tq)
-        sts8(sbase + NV_OFF_RSC + (32 * warp + 8 * h + 4 * mine + tq) * 32 + slot8 * 4 + (c >> 1),
-             rcode[tq]);
+      for (int k = 1; k < 4; ++k) {
+        const int src_b = (b + k) & 3;   // the lane this one reads
+        const uint32_t got = __shfl_sync(0xFFFFFFFFu, pick4(rcode, (b - k) & 3),
+                                         (lane & ~7) | (2 * src_b + mine));
+        word |= got << (8 * src_b);
+      }
+      sts32(sbase + NV_OFF_RSC + (32 * warp + 8 * h + 4 * mine + b) * NV_RSC_PITCH + slot8 * 4,
+            word);
     }
 
     // ---- transposed: block scales (split over the h pair), codes, scales ----
@@ -365,7 +402,7 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
       // Scale bytes: [64 columns][16 blocks of 16 rows].
 #pragma unroll
       for (int tq = 0; tq < 4; ++tq)
-        sts8(sbase + NV_OFF_TSC + (8 * c + 4 * mine + tq) * 16 + 2 * warp + (h >> 1), tcode[tq]);
+        sts8(sbase + NV_OFF_TSC + tsc_offset(8 * c + 4 * mine + tq, 2 * warp + (h >> 1)), tcode[tq]);
     }
 
     // ---- barrier B: staging complete --------------------------------------
@@ -386,10 +423,13 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         if (k < a.K) {
           uint8_t* dst = a.s_t + static_cast<size_t>(k) * nmb + mb0;
           const uint4 v = lds128(sbase + NV_OFF_TSC + kc * 16);
+          const uint32_t rot[4] = {v.x, v.y, v.z, v.w};
+          const int r = (kc >> 3) & 3;   // word j of the column is stored at (j + r) % 4
+          const uint32_t wv[4] = {pick4(rot, r), pick4(rot, (r + 1) & 3), pick4(rot, (r + 2) & 3),
+                                  pick4(rot, (r + 3) & 3)};
           if (nvalid == 16 && (nmb & 15) == 0) {
-            stg128(dst, v.x, v.y, v.z, v.w);
+            stg128(dst, wv[0], wv[1], wv[2], wv[3]);
           } else {
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
             for (int bb = 0; bb < nvalid; ++bb) stg8(dst + bb, (wv[bb >> 2] >> (8 * (bb & 3))) & 0xFFu);
           }
         }
@@ -432,11 +472,13 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         if (row < a.M) {
           const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
           uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
-          const uint32_t src = sbase + NV_OFF_RSC + tid * 32;
+          const uint32_t src = sbase + NV_OFF_RSC + tid * NV_RSC_PITCH;
           if (rs_first == 0 && slot8 == 7 && (nkb & 7) == 0) {
-            const uint4 lo = lds128(src), hi = lds128(src + 16);
-            stg128(dst, lo.x, lo.y, lo.z, lo.w);
-            stg128(dst + 16, hi.x, hi.y, hi.z, hi.w);
+            uint32_t w8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w8[q] = lds32(src + 4 * q);
+            stg128(dst, w8[0], w8[1], w8[2], w8[3]);
+            stg128(dst + 16, w8[4], w8[5], w8[6], w8[7]);
           } else {
             const int b_end = min((slot8 + 1) * 4, nkb - kb0);
             for (int bb = rs_first * 4; bb < b_end; ++bb)
