@@ -17,7 +17,7 @@ from . import build as _build
 
 ROWWISE, COLWISE, DBIAS = 1, 2, 4
 NVFP4_2D = 16
-ACT_NONE, ACT_GELU_TANH = 0, 1
+ACT_NONE, ACT_GELU_TANH, ACT_SILU = 0, 1, 2
 
 _lib = None
 
@@ -52,6 +52,20 @@ def lib():
         L.orc_gelu_tanh.argtypes = [ctypes.c_float]
         L.orc_swiglu.restype = ctypes.c_float
         L.orc_swiglu.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.orc_geglu.restype = ctypes.c_float
+        L.orc_geglu.argtypes = [ctypes.c_float, ctypes.c_float]
+        for name in ("orc_dgelu_tanh", "orc_dsilu"):
+            getattr(L, name).restype = ctypes.c_float
+            getattr(L, name).argtypes = [ctypes.c_float]
+        L.orc_mx_quantize_gated.restype = ctypes.c_int
+        L.orc_mx_quantize_gated.argtypes = [ctypes.c_void_p, i64, i64, i64, i64, ctypes.c_int,
+                                            ctypes.c_int, u8p, u8p, u8p, u8p]
+        L.orc_mx_quantize_dact.restype = ctypes.c_int
+        L.orc_mx_quantize_dact.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, i64, i64, i64,
+                                           ctypes.c_int, ctypes.c_int, u8p, u8p, u8p, u8p, f32p]
+        L.orc_mx_quantize_dgated.restype = ctypes.c_int
+        L.orc_mx_quantize_dgated.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, i64, i64, i64,
+                                             i64, ctypes.c_int, ctypes.c_int, u8p, u8p, u8p, u8p]
         L.orc_mx_quantize.restype = ctypes.c_int
         L.orc_mx_quantize.argtypes = [ctypes.c_void_p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                       u8p, u8p, u8p, u8p, f32p]
@@ -132,6 +146,18 @@ def swiglu(g, u):
     return float(lib().orc_swiglu(float(g), float(u)))
 
 
+def geglu(g, u):
+    return float(lib().orc_geglu(float(g), float(u)))
+
+
+def dgelu_tanh(x):
+    return float(lib().orc_dgelu_tanh(float(x)))
+
+
+def dsilu(x):
+    return float(lib().orc_dsilu(float(x)))
+
+
 # --------------------------------------------------------------------------
 # Whole-matrix quantizers
 # --------------------------------------------------------------------------
@@ -207,4 +233,67 @@ def nvfp4_quantize(x, tensor_amax=None, flags=ROWWISE | COLWISE):
     if rc != 0:
         raise ValueError(f"orc_nvfp4_quantize rejected M={M} K={K} ld={ld}")
     out["global_scale"] = float(g[0])
+    return out
+
+
+def _mx_outputs(M, K, flags):
+    out = {}
+    if flags & ROWWISE:
+        out["q_row"] = np.empty((M, K), np.uint8)
+        out["s_row"] = np.empty((M, K // 32), np.uint8)
+    if flags & COLWISE:
+        out["q_col"] = np.empty((K, M), np.uint8)
+        out["s_col"] = np.empty((K, M // 32), np.uint8)
+    if flags & DBIAS:
+        out["dbias"] = np.empty(K, np.float32)
+    return out
+
+
+def mx_quantize_gated(x, N, act=ACT_SILU, up_offset=None, flags=ROWWISE | COLWISE):
+    """Gated MXFP8: y = act(x[:, :N]) * x[:, up_offset:up_offset+N] with act
+    ACT_SILU (SwiGLU) or ACT_GELU_TANH (GeGLU); outputs as mx_quantize."""
+    p, M, W, ld = _matrix(x)
+    if up_offset is None:
+        up_offset = N
+    out = _mx_outputs(M, N, flags & (ROWWISE | COLWISE))
+    rc = lib().orc_mx_quantize_gated(p, M, N, ld, up_offset, flags, act,
+                                     _u8(out.get("q_row")), _u8(out.get("s_row")),
+                                     _u8(out.get("q_col")), _u8(out.get("s_col")))
+    if rc != 0:
+        raise ValueError(f"orc_mx_quantize_gated rejected M={M} N={N} ld={ld} act={act}")
+    return out
+
+
+def mx_quantize_dact(grad, x, act, flags=ROWWISE | COLWISE):
+    """Backward MXFP8: y = grad * act'(x) (act ACT_GELU_TANH or ACT_SILU),
+    quantized like mx_quantize; flags | DBIAS adds the column sums of y."""
+    pg, M, K, ldg = _matrix(grad)
+    px, M2, K2, ldx = _matrix(x)
+    if (M2, K2) != (M, K):
+        raise ValueError("grad and x shapes differ")
+    out = _mx_outputs(M, K, flags)
+    rc = lib().orc_mx_quantize_dact(pg, px, M, K, ldg, ldx, flags, act,
+                                    _u8(out.get("q_row")), _u8(out.get("s_row")),
+                                    _u8(out.get("q_col")), _u8(out.get("s_col")),
+                                    _f32(out.get("dbias")))
+    if rc != 0:
+        raise ValueError(f"orc_mx_quantize_dact rejected M={M} K={K} act={act}")
+    return out
+
+
+def mx_quantize_dgated(grad, x, N, act, up_offset=None, flags=ROWWISE | COLWISE):
+    """Backward gated MXFP8: grad [M, N], x = [gate | up]; y [M, 2N] =
+    [grad * up * act'(gate) | grad * act(gate)], quantized like mx_quantize."""
+    pg, M, Ng, ldg = _matrix(grad)
+    px, M2, W, ldx = _matrix(x)
+    if up_offset is None:
+        up_offset = N
+    if M2 != M or Ng != N:
+        raise ValueError("grad must be [M, N] for x = [gate | up]")
+    out = _mx_outputs(M, 2 * N, flags & (ROWWISE | COLWISE))
+    rc = lib().orc_mx_quantize_dgated(pg, px, M, N, ldg, ldx, up_offset, flags, act,
+                                      _u8(out.get("q_row")), _u8(out.get("s_row")),
+                                      _u8(out.get("q_col")), _u8(out.get("s_col")))
+    if rc != 0:
+        raise ValueError(f"orc_mx_quantize_dgated rejected M={M} N={N} act={act}")
     return out

@@ -30,7 +30,14 @@
  *  fusion "swiglu"): y is computed in double and rounded once to fp32, then
  *  quantized as above.  GELU is the tanh form
  *    0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)));
- *  SwiGLU is silu(g) * u with silu(g) = g / (1 + e^-g).
+ *  SwiGLU is silu(g) * u with silu(g) = g / (1 + e^-g); GeGLU (gated kernel
+ *  fusion "geglu") is gelu_tanh(g) * u.
+ *  Backward fusions (generic kernel fusions "dgelu", "dsilu", "dbias_dgelu";
+ *  gated kernel fusion "dswiglu", and its GeGLU counterpart): with grad the
+ *  incoming gradient, y = grad * act'(x) (dbias = column sums of y); for the
+ *  gated forms the output is [d gate | d up] = [grad * up * act'(gate) |
+ *  grad * act(gate)], 2N columns.  The derivatives are the closed forms
+ *  of the two functions above, evaluated in double.
  *
  *  dbias (TE PR #3291, fusion "dbias"): dbias[k] = sum over m of x[m][k],
  *  the exact sum rounded to fp32 (compensated summation in double).
@@ -212,6 +219,53 @@ float orc_swiglu(float gate, float up) {
     return (float)(silu * (double)up);
 }
 
+/* gelu_tanh(x) and its derivative in double.  With u = c (x + a x^3),
+ * s = e^(-2|u|):  tanh|u| = (1 - s) / (1 + s), so 1 + tanh(u) is 2 / (1 + s)
+ * for u >= 0 and 2 s / (1 + s) for u < 0, and 1 - tanh(u)^2 = 4 s / (1 + s)^2
+ * (no cancellation on either side).
+ *   d/dx 0.5 x (1 + tanh u) = 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) c (1 + 3 a x^2). */
+static void gelu_tanh_d(double x, double* value, double* deriv) {
+    const double c = sqrt(2.0 / ORC_PI), a = 0.044715;
+    double u = c * (x + a * x * x * x);
+    double s = exp(-2.0 * fabs(u));
+    double one_plus_tanh = (u >= 0.0) ? 2.0 / (1.0 + s) : 2.0 * s / (1.0 + s);
+    double sech2 = 4.0 * s / ((1.0 + s) * (1.0 + s));
+    if (value) *value = 0.5 * x * one_plus_tanh;
+    if (deriv) *deriv = 0.5 * one_plus_tanh + 0.5 * x * sech2 * c * (1.0 + 3.0 * a * x * x);
+}
+
+/* silu(x) = x sigma(x) and its derivative sigma(x) (1 + x sigma(-x)), in
+ * double (sigma(-x) = 1 - sigma(x) taken directly, no cancellation). */
+static void silu_d(double x, double* value, double* deriv) {
+    double sp = 1.0 / (1.0 + exp(-x));
+    double sm = 1.0 / (1.0 + exp(x));
+    if (value) *value = x * sp;
+    if (deriv) *deriv = sp * (1.0 + x * sm);
+}
+
+static void act_d(int act, double x, double* value, double* deriv) {
+    if (act == ORC_ACT_GELU_TANH) gelu_tanh_d(x, value, deriv);
+    else silu_d(x, value, deriv);
+}
+
+float orc_geglu(float gate, float up) {
+    double v;
+    gelu_tanh_d((double)gate, &v, NULL);
+    return (float)(v * (double)up);
+}
+
+float orc_dgelu_tanh(float x) {
+    double d;
+    gelu_tanh_d((double)x, NULL, &d);
+    return (float)d;
+}
+
+float orc_dsilu(float x) {
+    double d;
+    silu_d((double)x, NULL, &d);
+    return (float)d;
+}
+
 /* ------------------------------------------------------------------------ */
 /* MXFP8                                                                    */
 /* ------------------------------------------------------------------------ */
@@ -290,12 +344,13 @@ int orc_mx_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
     return 0;
 }
 
-int orc_mx_quantize_swiglu(const uint16_t* x, int64_t M, int64_t N,
-                           int64_t ldx, int64_t up_offset, int flags,
-                           uint8_t* q_row, uint8_t* s_row,
-                           uint8_t* q_col, uint8_t* s_col) {
+int orc_mx_quantize_gated(const uint16_t* x, int64_t M, int64_t N,
+                          int64_t ldx, int64_t up_offset, int flags, int act,
+                          uint8_t* q_row, uint8_t* s_row,
+                          uint8_t* q_col, uint8_t* s_col) {
     if (!x || M < 0 || N < 0 || up_offset < N || ldx < up_offset + N) return -1;
     if ((M % 32) || (N % 32)) return -1;
+    if (act != ORC_ACT_SILU && act != ORC_ACT_GELU_TANH) return -1;
     if (M == 0 || N == 0) return 0;
     float* y = (float*)malloc((size_t)(M * N) * sizeof(float));
     if (!y) return -1;
@@ -303,9 +358,71 @@ int orc_mx_quantize_swiglu(const uint16_t* x, int64_t M, int64_t N,
         for (int64_t n = 0; n < N; ++n) {
             float g = (float)orc_bf16_decode(x[m * ldx + n]);
             float u = (float)orc_bf16_decode(x[m * ldx + up_offset + n]);
-            y[m * N + n] = orc_swiglu(g, u);
+            y[m * N + n] = (act == ORC_ACT_SILU) ? orc_swiglu(g, u) : orc_geglu(g, u);
         }
     mx_quantize_dense(y, M, N, flags, q_row, s_row, q_col, s_col);
+    free(y);
+    return 0;
+}
+
+int orc_mx_quantize_swiglu(const uint16_t* x, int64_t M, int64_t N,
+                           int64_t ldx, int64_t up_offset, int flags,
+                           uint8_t* q_row, uint8_t* s_row,
+                           uint8_t* q_col, uint8_t* s_col) {
+    return orc_mx_quantize_gated(x, M, N, ldx, up_offset, flags, ORC_ACT_SILU,
+                                 q_row, s_row, q_col, s_col);
+}
+
+int orc_mx_quantize_dact(const uint16_t* grad, const uint16_t* x, int64_t M, int64_t K,
+                         int64_t ldg, int64_t ldx, int flags, int act,
+                         uint8_t* q_row, uint8_t* s_row,
+                         uint8_t* q_col, uint8_t* s_col, float* dbias) {
+    if (!grad || !x || M < 0 || K < 0 || ldg < K || ldx < K) return -1;
+    if ((M % 32) || (K % 32)) return -1;
+    if (act != ORC_ACT_SILU && act != ORC_ACT_GELU_TANH) return -1;
+    if (M == 0 || K == 0) {
+        if ((flags & ORC_DBIAS) && dbias)
+            for (int64_t k = 0; k < K; ++k) dbias[k] = 0.0f;
+        return 0;
+    }
+    float* y = (float*)malloc((size_t)(M * K) * sizeof(float));
+    if (!y) return -1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            double d;
+            act_d(act, orc_bf16_decode(x[m * ldx + k]), NULL, &d);
+            y[m * K + k] = (float)(orc_bf16_decode(grad[m * ldg + k]) * d);
+        }
+    mx_quantize_dense(y, M, K, flags, q_row, s_row, q_col, s_col);
+    if ((flags & ORC_DBIAS) && dbias)
+        for (int64_t k = 0; k < K; ++k) dbias[k] = column_sum(y, M, K, k);
+    free(y);
+    return 0;
+}
+
+int orc_mx_quantize_dgated(const uint16_t* grad, const uint16_t* x, int64_t M, int64_t N,
+                           int64_t ldg, int64_t ldx, int64_t up_offset, int flags, int act,
+                           uint8_t* q_row, uint8_t* s_row,
+                           uint8_t* q_col, uint8_t* s_col) {
+    if (!grad || !x || M < 0 || N < 0 || ldg < N || up_offset < N || ldx < up_offset + N)
+        return -1;
+    if ((M % 32) || (N % 32)) return -1;
+    if (act != ORC_ACT_SILU && act != ORC_ACT_GELU_TANH) return -1;
+    if (M == 0 || N == 0) return 0;
+    const int64_t W = 2 * N;
+    float* y = (float*)malloc((size_t)(M * W) * sizeof(float));
+    if (!y) return -1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double g = orc_bf16_decode(grad[m * ldg + n]);
+            double gate = orc_bf16_decode(x[m * ldx + n]);
+            double up = orc_bf16_decode(x[m * ldx + up_offset + n]);
+            double v, d;
+            act_d(act, gate, &v, &d);
+            y[m * W + n] = (float)(g * up * d);       /* d / d gate */
+            y[m * W + N + n] = (float)(g * v);        /* d / d up   */
+        }
+    mx_quantize_dense(y, M, W, flags, q_row, s_row, q_col, s_col);
     free(y);
     return 0;
 }

@@ -34,7 +34,7 @@ extern "C" {
 #endif
 
 enum { ORC_ROWWISE = 1, ORC_COLWISE = 2, ORC_DBIAS = 4, ORC_NVFP4_2D = 16 };
-enum { ORC_ACT_NONE = 0, ORC_ACT_GELU_TANH = 1 };
+enum { ORC_ACT_NONE = 0, ORC_ACT_GELU_TANH = 1, ORC_ACT_SILU = 2 };
 
 /* Scalar format conversions. */
 double  orc_bf16_decode(uint16_t bits);
@@ -49,9 +49,12 @@ void orc_e4m3_encode_array(const double* v, int64_t n, uint8_t* out);
 void orc_e2m1_encode_array(const double* v, int64_t n, uint8_t* out);
 void orc_e8m0_code_array(const double* amax, int64_t n, uint8_t* out);
 
-/* Activations evaluated in double and rounded once to fp32. */
+/* Activations and derivatives evaluated in double and rounded once to fp32. */
 float orc_gelu_tanh(float x);
 float orc_swiglu(float gate, float up);
+float orc_geglu(float gate, float up);
+float orc_dgelu_tanh(float x);
+float orc_dsilu(float x);
 
 /* MXFP8 quantization of a bf16 matrix x[M][K] (row stride ldx elements).
  * flags: ORC_ROWWISE / ORC_COLWISE select the outputs; ORC_DBIAS writes
@@ -66,6 +69,27 @@ int orc_mx_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
  * n < N, then the same rowwise/colwise quantization of y. */
 int orc_mx_quantize_swiglu(const uint16_t* x, int64_t M, int64_t N,
                            int64_t ldx, int64_t up_offset, int flags,
+                           uint8_t* q_row, uint8_t* s_row,
+                           uint8_t* q_col, uint8_t* s_col);
+
+/* Gated MXFP8 with act ORC_ACT_SILU (SwiGLU) or ORC_ACT_GELU_TANH (GeGLU):
+ * y[m][n] = act(gate) * up, gate = x[m][n], up = x[m][n + up_offset]. */
+int orc_mx_quantize_gated(const uint16_t* x, int64_t M, int64_t N,
+                          int64_t ldx, int64_t up_offset, int flags, int act,
+                          uint8_t* q_row, uint8_t* s_row,
+                          uint8_t* q_col, uint8_t* s_col);
+
+/* Backward MXFP8: y = grad * act'(x) (act ORC_ACT_GELU_TANH or ORC_ACT_SILU),
+ * product in double rounded once; ORC_DBIAS writes the column sums of y. */
+int orc_mx_quantize_dact(const uint16_t* grad, const uint16_t* x, int64_t M, int64_t K,
+                         int64_t ldg, int64_t ldx, int flags, int act,
+                         uint8_t* q_row, uint8_t* s_row,
+                         uint8_t* q_col, uint8_t* s_col, float* dbias);
+
+/* Backward gated MXFP8: grad [M][N], x = [gate | up] as for the gated
+ * forward; y [M][2N] = [grad * up * act'(gate) | grad * act(gate)]. */
+int orc_mx_quantize_dgated(const uint16_t* grad, const uint16_t* x, int64_t M, int64_t N,
+                           int64_t ldg, int64_t ldx, int64_t up_offset, int flags, int act,
                            uint8_t* q_row, uint8_t* s_row,
                            uint8_t* q_col, uint8_t* s_col);
 

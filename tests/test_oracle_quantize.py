@@ -229,6 +229,98 @@ def test_activation_quantize_composes():
     _check_blocks(yg, outg)
 
 
+def _richardson(f, x, h):
+    """Derivative of f at x by central differences with one Richardson step
+    (error O(h^4)), in float64."""
+    d1 = (f(x + h) - f(x - h)) / (2 * h)
+    d2 = (f(x + h / 2) - f(x - h / 2)) / h
+    return (4 * d2 - d1) / 3
+
+
+def _gelu64(x):
+    return 0.5 * x * (1 + np.tanh(np.sqrt(2 / np.pi) * (x + 0.044715 * x ** 3)))
+
+
+def _silu64(x):
+    return x / (1 + np.exp(-x))
+
+
+def test_activation_derivatives():
+    """dgelu / dsilu against numerical differentiation of the functions
+    themselves, plus the values the closed forms fix: 1/2 at 0, 1 far right,
+    0 far left (the GELU derivative dips just below 0 before it)."""
+    rng = np.random.default_rng(16)
+    xs = np.concatenate([rng.standard_normal(3000) * 3,
+                         np.linspace(-6, 6, 241)]).astype(np.float32)
+    for f64, d_or in ((_gelu64, oracle.dgelu_tanh), (_silu64, oracle.dsilu)):
+        for x in xs:
+            xd = float(x)
+            want = _richardson(f64, xd, 1e-2 * max(1.0, abs(xd)))
+            got = d_or(x)
+            assert abs(got - want) <= 2e-7 * max(1.0, abs(want)), (d_or.__name__, xd, got, want)
+    assert oracle.dgelu_tanh(0.0) == 0.5 and oracle.dsilu(0.0) == 0.5
+    assert oracle.dgelu_tanh(20.0) == 1.0 and oracle.dsilu(40.0) == 1.0
+    assert abs(oracle.dgelu_tanh(-20.0)) < 1e-30 and abs(oracle.dsilu(-110.0)) < 1e-30
+    assert min(oracle.dgelu_tanh(x) for x in np.linspace(-3, -1, 81)) < 0   # the dip
+
+
+def test_geglu_reduces_to_gelu():
+    """GeGLU with up = 1 is GELU of the gate (the pinned GELU path), bit for
+    bit; up = 2 doubles every value, so the codes stay and each scale code
+    moves up by one."""
+    gate = synth.gelu(M=64, K=96, seed=17)
+    ones = np.full_like(gate, 0x3F80)                      # bf16 1.0
+    twos = np.full_like(gate, 0x4000)                      # bf16 2.0
+    ref = oracle.mx_quantize(gate, oracle.ROWWISE | oracle.COLWISE, act=oracle.ACT_GELU_TANH)
+    got = oracle.mx_quantize_gated(np.hstack([gate, ones]), 96, act=oracle.ACT_GELU_TANH)
+    for key in ref:
+        np.testing.assert_array_equal(got[key], ref[key])
+    dbl = oracle.mx_quantize_gated(np.hstack([gate, twos]), 96, act=oracle.ACT_GELU_TANH)
+    np.testing.assert_array_equal(dbl["q_row"], ref["q_row"])
+    nz = ref["s_row"] > 0
+    np.testing.assert_array_equal(dbl["s_row"][nz], ref["s_row"][nz] + 1)
+
+
+def test_dact_quantize_composes():
+    """y = grad * act'(x) with grad a power of two (so the product is the
+    exactly scaled fp32 derivative), then the block rule built here from the
+    pinned encoders; dbias = exact column sums of y."""
+    x = synth.gelu(M=64, K=64, seed=18)
+    rng = np.random.default_rng(19)
+    gvals = rng.choice(np.array([1.0, -1.0, 2.0, -0.5, 0.25, 4.0], np.float32), size=(64, 64))
+    grad = bf16(gvals)
+    xf = synth.bf16_bits_to_f32(x)
+    for act, d in ((oracle.ACT_GELU_TANH, oracle.dgelu_tanh), (oracle.ACT_SILU, oracle.dsilu)):
+        out = oracle.mx_quantize_dact(grad, x, act, oracle.ROWWISE | oracle.COLWISE | oracle.DBIAS)
+        y = np.array([[np.float32(gvals[m, k]) * np.float32(d(xf[m, k])) for k in range(64)]
+                      for m in range(64)], np.float32)
+        _check_blocks(y.astype(np.float64), out)
+        want = np.array([np.float32(math.fsum(y[:, k].astype(np.float64))) for k in range(64)])
+        np.testing.assert_array_equal(out["dbias"], want)
+
+
+def test_dgated_halves():
+    """With grad = 1 and up = 1, the d-gate half of the backward gated output
+    is act'(gate) (the pinned dact path) and the d-up half is act(gate) (the
+    pinned gated forward with up = 1); the halves are whole 32-column blocks
+    rowwise and whole code rows colwise."""
+    gate = synth.gelu(M=64, K=64, seed=20)
+    ones = np.full_like(gate, 0x3F80)
+    x = np.hstack([gate, ones])
+    for act in (oracle.ACT_SILU, oracle.ACT_GELU_TANH):
+        out = oracle.mx_quantize_dgated(ones, x, 64, act)
+        dact = oracle.mx_quantize_dact(ones, gate, act)
+        fwd = oracle.mx_quantize_gated(x, 64, act=act)
+        np.testing.assert_array_equal(out["q_row"][:, :64], dact["q_row"])
+        np.testing.assert_array_equal(out["s_row"][:, :2], dact["s_row"])
+        np.testing.assert_array_equal(out["q_col"][:64], dact["q_col"])
+        np.testing.assert_array_equal(out["s_col"][:64], dact["s_col"])
+        np.testing.assert_array_equal(out["q_row"][:, 64:], fwd["q_row"])
+        np.testing.assert_array_equal(out["s_row"][:, 2:], fwd["s_row"])
+        np.testing.assert_array_equal(out["q_col"][64:], fwd["q_col"])
+        np.testing.assert_array_equal(out["s_col"][64:], fwd["s_col"])
+
+
 def _check_blocks(y, out):
     M, K = y.shape
     for m in range(M):
