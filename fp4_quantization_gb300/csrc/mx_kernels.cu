@@ -542,7 +542,8 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
           const int kb0 = (tk - slot) * 4;   // first k-block of the group
           uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
           const uint32_t src = sbase + L::OFF_RSC + (pos.bi * BAND + rr) * 32;
-          if (rsc_first == 0 && slot == 7 && (nkb & 7) == 0) {
+          // Two 16-byte stores: every row start must be 16-byte aligned.
+          if (rsc_first == 0 && slot == 7 && (nkb & 15) == 0) {
             const uint4 lo = lds128(src), hi = lds128(src + 16);
             stg128(dst, lo.x, lo.y, lo.z, lo.w);
             stg128(dst + 16, hi.x, hi.y, hi.z, hi.w);

@@ -473,7 +473,8 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
           const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
           uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
           const uint32_t src = sbase + NV_OFF_RSC + tid * NV_RSC_PITCH;
-          if (rs_first == 0 && slot8 == 7 && (nkb & 7) == 0) {
+          // Two 16-byte stores: every row start must be 16-byte aligned.
+          if (rs_first == 0 && slot8 == 7 && (nkb & 15) == 0) {
             uint32_t w8[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) w8[q] = lds32(src + 4 * q);

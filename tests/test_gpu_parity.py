@@ -43,15 +43,17 @@ def test_mx_rowcol_bit_exact(name, bits, _, flags):
         assert_equal_bytes(host(out[key]), ref[key], f"{name} {key}")
 
 
-@pytest.mark.parametrize("M,K,seed", [(3104, 2080, 48), (8192, 4096, 49)],
-                         ids=["ragged_groups", "whole_groups"])
+@pytest.mark.parametrize("M,K,seed", [(3104, 2080, 48), (8192, 4096, 49), (16384, 1280, 60)],
+                         ids=["ragged_groups", "whole_groups", "scale_rows_8_aligned"])
 @pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
 def test_mx_rowcol_cta_ranges(M, K, seed, flags):
     """Enough 128x128 steps that every SM walks a range of them: the first
     shape has a ragged last band group and ragged K, with CTA ranges of two
     or three steps that start and end inside band groups; the second gives
     each CTA about thirteen steps, so some ranges cover whole groups and
-    their scale bytes leave in full runs."""
+    their scale bytes leave in full runs; the third has rowwise scale rows of
+    40 bytes (8- but not 16-byte aligned), whose full 8-step runs must not
+    take the 16-byte store path."""
     bits = synth.rowcol(M=M, K=K, seed=seed)
     x = to_device(bits)
     dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -131,7 +133,7 @@ def test_mx_swiglu_row_only_and_col_only():
 
 
 @pytest.mark.parametrize("M,K,seed", [(224, 160, 44), (32, 32, 45), (64, 64, 46), (512, 320, 47),
-                                      (768, 1600, 48)])
+                                      (768, 1600, 48), (32768, 640, 61)])
 @pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
 def test_nvfp4_bit_exact(M, K, seed, flags):
     bits = synth.nvfp4(M=M, K=K, seed=seed)
@@ -195,7 +197,7 @@ def test_nvfp4_zero_tensor():
 
 
 @pytest.mark.parametrize("M,K,seed", [(224, 160, 53), (32, 32, 54), (512, 320, 55),
-                                      (768, 1600, 56), (3104, 2080, 57)])
+                                      (768, 1600, 56), (3104, 2080, 57), (32768, 640, 59)])
 @pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
 def test_nvfp4_2d_bit_exact(M, K, seed, flags):
     """16x16 blocks: several CTA steps, ragged bands and ranges."""
