@@ -50,6 +50,13 @@ def mx_bytes(M, K, rowwise=True, colwise=True, dbias=False, gated=False):
     return read + written
 
 
+def dgated_bytes(M, N, rowwise=True, colwise=True):
+    """Gated backward: grad [M, N] and x [M, 2N] bf16 read, codes and scales
+    of the [M, 2N] output written."""
+    per_dir = 2 * M * N + 2 * M * N // 32
+    return M * N * 2 + M * 2 * N * 2 + per_dir * (int(rowwise) + int(colwise))
+
+
 def nvfp4_bytes(M, K, rowwise=True, colwise=True):
     """bf16 input + packed E2M1 codes + E4M3 scales, plus the fp32 tensor
     amax read and the fp32 global scale written."""
@@ -259,6 +266,18 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
         ("gelu_rowcol_8192x14336", lambda: synth.gelu(),
          lambda x, o: mxq.mx_quantize_rowcol(x, mxq.ROWWISE | mxq.COLWISE | mxq.ACT_GELU_TANH, **o),
          mx_bytes(8192, 14336), {}),
+        ("geglu_rowcol_8192x2x14336", lambda: synth.swiglu(),
+         lambda x, o: mxq.mx_quantize_gated(x, mxq.ROWWISE | mxq.COLWISE | mxq.ACT_GELU_TANH, **o),
+         mx_bytes(8192, 14336, gated=True), {}),
+        ("dbias_dgelu_rowcol_8192x14336",
+         lambda: (synth.gelu(seed=8), synth.gelu()),
+         lambda x, o: mxq.mx_quantize_dact(x[0], x[1], mxq.ROWWISE | mxq.COLWISE | mxq.DBIAS
+                                           | mxq.ACT_GELU_TANH, **o),
+         mx_bytes(8192, 14336, gated=True, dbias=True), {}),
+        ("dswiglu_rowcol_8192x14336",
+         lambda: (synth.gelu(seed=9), synth.swiglu()),
+         lambda x, o: mxq.mx_quantize_dgated(x[0], x[1], mxq.ROWWISE | mxq.COLWISE, **o),
+         dgated_bytes(8192, 14336), {}),
         ("nvfp4_rowtrans_16384x8192", lambda: synth.nvfp4(),
          lambda x, o: mxq.nvfp4_quantize_transpose(x, mxq.ROWWISE | mxq.COLWISE, **o),
          nvfp4_bytes(16384, 8192), {}),
@@ -279,7 +298,9 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
     for name, gen, call, nbytes, _ in cases:
         if only is not None and name != only:
             continue
-        x = to_device(gen(), device)
+        data = gen()
+        x = (tuple(to_device(d, device) for d in data) if isinstance(data, tuple)
+             else to_device(data, device))
         first = call(x, {})                       # allocates the outputs once
         if name.startswith("bf16_amax"):
             keep = {"out": first}
@@ -289,9 +310,13 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
             keep["amax"] = mxq.bf16_amax(x)
         elif name.startswith("nvfp4"):
             keep["workspace"] = torch.empty(16, dtype=torch.uint8, device=device)
-        if name.startswith("dbias"):
+        if name.startswith("dbias_rowcol"):
             keep["workspace"] = torch.empty(
                 max(16, mxq.mxq_workspace_bytes(mxq.OP_ROWCOL, 8192, 8192, 7)), dtype=torch.uint8,
+                device=device)
+        if name.startswith("dbias_dgelu"):
+            keep["workspace"] = torch.empty(
+                max(16, mxq.mxq_workspace_bytes(mxq.OP_DACT, 8192, 14336, 7)), dtype=torch.uint8,
                 device=device)
         total, per_call, _ = time_device(lambda: call(x, keep), steps, warmup, world, stream)
         avg_ms = total / steps

@@ -19,8 +19,10 @@ COLWISE = 2
 DBIAS = 4
 ACT_GELU_TANH = 8
 NVFP4_2D = 16
+ACT_SILU = 32
 OP_ROWCOL = 0
 OP_NVFP4 = 1
+OP_DACT = 2
 DEVERR_TIMEOUT = 1
 
 STATUS_NAMES = {0: "MXQ_OK", 1: "MXQ_EINVAL", 2: "MXQ_ESHAPE", 3: "MXQ_EALIGN",
@@ -129,8 +131,9 @@ def mx_quantize_rowcol_dbias_noalloc(x, flags=ROWWISE | COLWISE, *, q_row=None, 
 
 def mx_quantize_gated(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_col=None,
                       s_col=None, dev_err=None, stream=None):
-    """SwiGLU-gated MXFP8 of x[M, 2N] = [gate | up]; y = silu(gate) * up
-    in fp32, quantized like mx_quantize_rowcol (outputs sized by N)."""
+    """Gated MXFP8 of x[M, 2N] = [gate | up]; y = silu(gate) * up (SwiGLU,
+    the default) or gelu_tanh(gate) * up (flags | ACT_GELU_TANH: GeGLU) in
+    fp32, quantized like mx_quantize_rowcol (outputs sized by N)."""
     ldx = _input(x)
     M, W = x.shape
     if W % 2:
@@ -148,6 +151,65 @@ def mx_quantize_gated(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_c
         _ptr(x), M, N, ldx, flags, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
         _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(dev_err), _stream(stream))
     _check(st, "mx_quantize_gated")
+    return out
+
+
+def _mx_outputs(M, K, flags, dev, q_row, s_row, q_col, s_col):
+    out = {}
+    if flags & ROWWISE:
+        out["q_row"] = q_row if q_row is not None else _empty((M, K), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty((M, K // 32), torch.uint8, dev)
+    if flags & COLWISE:
+        out["q_col"] = q_col if q_col is not None else _empty((K, M), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty((K, M // 32), torch.uint8, dev)
+    return out
+
+
+def mx_quantize_dact(grad, x, flags, *, q_row=None, s_row=None, q_col=None, s_col=None,
+                     dbias=None, workspace=None, dev_err=None, stream=None):
+    """Backward MXFP8: y = grad * act'(x) for grad, x [M, K] bf16, with act
+    gelu_tanh (flags | ACT_GELU_TANH) or silu (flags | ACT_SILU); outputs as
+    mx_quantize_rowcol, dbias = column sums of y with DBIAS."""
+    ldg = _input(grad, "grad")
+    ldx = _input(x)
+    M, K = x.shape
+    if tuple(grad.shape) != (M, K):
+        raise ValueError("grad and x shapes differ")
+    dev = x.device
+    out = _mx_outputs(M, K, flags, dev, q_row, s_row, q_col, s_col)
+    ws_bytes = 0
+    if flags & DBIAS:
+        out["dbias"] = dbias if dbias is not None else _empty((K,), torch.float32, dev)
+        if workspace is None:
+            need = mxq_workspace_bytes(OP_DACT, M, K, flags)
+            workspace = _empty((max(need, 16),), torch.uint8, dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = _lib.lib().mx_quantize_dact(
+        _ptr(grad), _ptr(x), M, K, ldg, ldx, flags, _ptr(out.get("q_row")),
+        _ptr(out.get("s_row")), _ptr(out.get("q_col")), _ptr(out.get("s_col")),
+        _ptr(out.get("dbias")), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream))
+    _check(st, "mx_quantize_dact")
+    return out
+
+
+def mx_quantize_dgated(grad, x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_col=None,
+                       s_col=None, dev_err=None, stream=None):
+    """Backward of the gated activation: grad [M, N], x [M, 2N] = [gate |
+    up]; y [M, 2N] = [grad * up * act'(gate) | grad * act(gate)] with act
+    silu (default) or gelu_tanh (flags | ACT_GELU_TANH), quantized like
+    mx_quantize_rowcol (outputs sized by 2N)."""
+    ldg = _input(grad, "grad")
+    ldx = _input(x)
+    M, W = x.shape
+    if W % 2 or tuple(grad.shape) != (M, W // 2):
+        raise ValueError("x must be [M, 2N] = [gate | up] and grad [M, N]")
+    N = W // 2
+    out = _mx_outputs(M, W, flags, x.device, q_row, s_row, q_col, s_col)
+    st = _lib.lib().mx_quantize_dgated(
+        _ptr(grad), _ptr(x), M, N, ldg, ldx, flags, _ptr(out.get("q_row")),
+        _ptr(out.get("s_row")), _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(dev_err),
+        _stream(stream))
+    _check(st, "mx_quantize_dgated")
     return out
 
 

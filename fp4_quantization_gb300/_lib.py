@@ -26,6 +26,10 @@ SIGNATURES = {
                                                         _vp, _vp, _vp, _vp, _vp]),
     "mx_quantize_gated": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _vp, _vp,
                                          _vp]),
+    "mx_quantize_dact": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _u32, _vp, _vp, _vp,
+                                        _vp, _vp, _vp, _sz, _vp, _vp]),
+    "mx_quantize_dgated": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _u32, _vp, _vp, _vp,
+                                          _vp, _vp, _vp]),
     "bf16_amax": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp]),
     "nvfp4_quantize_transpose": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _vp,
                                                 _vp, _vp, _vp, _sz, _vp, _vp]),

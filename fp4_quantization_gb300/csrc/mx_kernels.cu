@@ -83,6 +83,70 @@ __device__ __forceinline__ float swiglu_f32(float g, float u) {
   return g * rcp_approx(1.0f + e) * u;
 }
 
+// gelu_tanh(x) and its derivative
+//   0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) sqrt(2/pi) (1 + 3 * 0.044715 x^2),
+// both from s = e^(-2|u|) in (0, 1]: 1 + tanh u is 2 / (1 + s) for u >= 0 and
+// 2 s / (1 + s) below, 1 - tanh^2 u = 4 s / (1 + s)^2 (no cancellation, no
+// overflow).
+__device__ __forceinline__ void gelu_tanh_d_f32(float x, float& value, float& deriv) {
+  constexpr float kC = 0.7978845608028654f;                       // sqrt(2 / pi)
+  constexpr float kNeg2Log2e = -2.0f * 1.4426950408889634f;
+  const float x2 = x * x;
+  const float u = kC * x * fmaf(0.044715f, x2, 1.0f);
+  const float sv = ex2_approx(kNeg2Log2e * fabsf(u));
+  const float r = rcp_approx(1.0f + sv);
+  const float one_plus_tanh = (u >= 0.0f ? 2.0f : 2.0f * sv) * r;
+  const float sech2 = 4.0f * sv * r * r;
+  value = 0.5f * x * one_plus_tanh;
+  deriv = fmaf(0.5f * x * sech2 * kC, fmaf(3.0f * 0.044715f, x2, 1.0f), 0.5f * one_plus_tanh);
+}
+
+// silu(x) = x sigma(x) and its derivative sigma(x) (1 + x sigma(-x)), from
+// t = e^(-|x|) in (0, 1] (sigma of the negative side is t / (1 + t)).
+__device__ __forceinline__ void silu_d_f32(float x, float& value, float& deriv) {
+  constexpr float kNegLog2e = -1.4426950408889634f;
+  const float t = ex2_approx(kNegLog2e * fabsf(x));
+  const float r = rcp_approx(1.0f + t);
+  const float sp = x >= 0.0f ? r : t * r;     // sigma(x)
+  const float sm = x >= 0.0f ? t * r : r;     // sigma(-x)
+  value = x * sp;
+  deriv = sp * fmaf(x, sm, 1.0f);
+}
+
+// Operand tiles per step and output tiles per step of each activation.
+__host__ __device__ constexpr int act_operands(int act) {
+  return act == ACT_NONE || act == ACT_GELU ? 1
+         : (act == ACT_DSWIGLU || act == ACT_DGEGLU) ? 3 : 2;
+}
+__host__ __device__ constexpr int act_outputs(int act) {
+  return (act == ACT_DSWIGLU || act == ACT_DGEGLU) ? 2 : 1;
+}
+
+// y of output t from the operands of one element: x (plain / GELU), gate and
+// up (SwiGLU / GeGLU), grad and x (dGELU / dSiLU), grad, gate and up (the
+// gated backward: t = 0 is d gate = grad * up * act'(gate), t = 1 is
+// d up = grad * act(gate)).
+template <int ACT>
+__device__ __forceinline__ float act_value(float o0, float o1, float o2, int t) {
+  if constexpr (ACT == ACT_GELU) {
+    return gelu_tanh_f32(o0);
+  } else if constexpr (ACT == ACT_SWIGLU) {
+    return swiglu_f32(o0, o1);
+  } else if constexpr (ACT == ACT_GEGLU) {
+    return gelu_tanh_f32(o0) * o1;
+  } else if constexpr (ACT == ACT_DGELU || ACT == ACT_DSILU) {
+    float v, d;
+    if constexpr (ACT == ACT_DGELU) gelu_tanh_d_f32(o1, v, d);
+    else silu_d_f32(o1, v, d);
+    return o0 * d;
+  } else {
+    float v, d;
+    if constexpr (ACT == ACT_DGEGLU) gelu_tanh_d_f32(o1, v, d);
+    else silu_d_f32(o1, v, d);
+    return t == 0 ? o0 * o2 * d : o0 * v;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Small helpers
 // ---------------------------------------------------------------------------
@@ -108,7 +172,7 @@ __device__ __forceinline__ void bar_sync_cta(int threads) {
 // Shared-memory layout of one CTA
 // ---------------------------------------------------------------------------
 
-template <int WARPS, int OPERANDS, int NSTAGES, int GROUP, int QBUF, int CPITCH>
+template <int WARPS, int OPERANDS, int NSTAGES, int GROUP, int QBUF, int CPITCH, int NOUT>
 struct MxLayout {
   static constexpr int BAND = 16 * WARPS;
   static constexpr int BPB = BAND / 32;                              // colwise blocks per band
@@ -119,14 +183,14 @@ struct MxLayout {
   static constexpr int QCOL_HALVES = BAND / 128;
   static constexpr int QCOL_BUF = QCOL_HALVES * QCOL_HALF;            // one step's codes
   static constexpr int OFF_QCOL = STAGES * STAGE_BYTES;              // 1024-aligned
-  // [GROUP bands][BAND rows][8 steps][4 blocks]
+  // [NOUT outputs][GROUP bands][BAND rows][8 steps][4 blocks]
   static constexpr int OFF_RSC = OFF_QCOL + QBUF * QCOL_BUF;
   // Colwise scale bytes, GROUP * BPB blocks of 128 columns: [128 columns]
   // [CPITCH bytes] when there are four blocks (one 4-byte word per column),
   // else [blocks][128 columns].
   static constexpr bool CSC_BY_COL = GROUP * BPB == 4;
   static_assert(CPITCH == 4 || CPITCH == 8, "column pitch of the scale staging");
-  static constexpr int OFF_CSC = OFF_RSC + GROUP * BAND * 32;
+  static constexpr int OFF_CSC = OFF_RSC + NOUT * GROUP * BAND * 32;
   static constexpr int CSC_BYTES = CSC_BY_COL ? MX_TILE_K * CPITCH : GROUP * BPB * MX_TILE_K;
   static constexpr int OFF_DB = OFF_CSC + CSC_BYTES;                 // [WARPS][128] fp32
   static constexpr int OFF_XCH = OFF_DB + WARPS * MX_TILE_K * 4;     // [WARPS][16][4] u32
@@ -145,15 +209,20 @@ template <int MODE, bool DBIAS, int ACT, int WARPS, int STAGES, int GROUP, int Q
           int CPITCH>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_qcol, const MxArgs a) {
+                   const __grid_constant__ CUtensorMap tmap_x2,
+                   const __grid_constant__ CUtensorMap tmap_qcol,
+                   const __grid_constant__ CUtensorMap tmap_qcol2, const MxArgs a) {
   constexpr bool ROW = (MODE & MX_ROW) != 0;
   constexpr bool COL = (MODE & MX_COL) != 0;
-  constexpr int OPERANDS = (ACT == ACT_SWIGLU) ? 2 : 1;
-  using L = MxLayout<WARPS, OPERANDS, STAGES, GROUP, QBUF, CPITCH>;
+  constexpr int OPERANDS = act_operands(ACT);
+  constexpr int NOUT = act_outputs(ACT);
+  using L = MxLayout<WARPS, OPERANDS, STAGES, GROUP, QBUF, CPITCH, NOUT>;
   constexpr int THREADS = WARPS * 32;
   constexpr int BAND = L::BAND;
   constexpr int ROW_PITCH = MX_TILE_K * 2;   // bf16 tile row, bytes
-  static_assert(!(DBIAS && ACT != ACT_NONE), "dbias is defined on the plain path only");
+  static_assert(!DBIAS || ACT == ACT_NONE || ACT == ACT_DGELU || ACT == ACT_DSILU,
+                "dbias is defined on the plain and single-input backward paths");
+  static_assert(NOUT == 1 || GROUP == 1, "two-output steps keep one band per CTA");
   static_assert(BAND % 128 == 0 && BAND <= 256, "colwise codes leave in 128-row halves");
 
   extern __shared__ uint8_t smem_raw[];
@@ -216,15 +285,20 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     mbar_arrive_expect_tx(bar0 + 8 * s, L::STAGE_BYTES);
     tma_load_2d_hint(dst, &tmap_x, lpos.tk * MX_TILE_K, lpos.band() * BAND, bar0 + 8 * s,
                      load_policy);
-    if (OPERANDS == 2)
-      tma_load_2d_hint(dst + L::TILE_BYTES, &tmap_x, a.up_col + lpos.tk * MX_TILE_K,
+    if (OPERANDS >= 2)
+      tma_load_2d_hint(dst + L::TILE_BYTES, &tmap_x2, a.up_col + lpos.tk * MX_TILE_K,
+                       lpos.band() * BAND, bar0 + 8 * s, load_policy);
+    if (OPERANDS >= 3)
+      tma_load_2d_hint(dst + 2 * L::TILE_BYTES, &tmap_x2, a.up_col2 + lpos.tk * MX_TILE_K,
                        lpos.band() * BAND, bar0 + 8 * s, load_policy);
     lpos.advance(a.tiles_m, a.tiles_k);
   };
 
   if (tid == 0) {
     prefetch_tensormap(&tmap_x);
+    if (OPERANDS >= 2) prefetch_tensormap(&tmap_x2);
     if (COL) prefetch_tensormap(&tmap_qcol);
+    if (COL && NOUT == 2) prefetch_tensormap(&tmap_qcol2);
 #pragma unroll
     for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
     fence_barrier_init();
@@ -242,336 +316,341 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int tk = pos.tk;
     const bool ok = mbar_wait_bounded(bar0 + 8 * s, (j / STAGES) & 1, a.timeout_ns);
 
-    const uint32_t my_row0 =
-        sbase + s * L::STAGE_BYTES + (16 * warp + 8 * h) * ROW_PITCH + c * 16;
+    // One pass per output tile of the step (two for the gated backward,
+    // which writes d gate and d up from the same loaded tiles).
+    for (int t = 0; t < NOUT; ++t) {
+      const uint32_t my_row0 =
+          sbase + s * L::STAGE_BYTES + (16 * warp + 8 * h) * ROW_PITCH + c * 16;
 
-    // ---- load this lane's 8 x 8 block and reduce it to magnitude maxima ---
-    // The plain path keeps the packed bf16 pairs (xr) and widens them where
-    // they are used; the activation paths hold y in fp32.  ce[p] / re[q]:
-    // exponent fields of the largest magnitudes of columns 2p, 2p+1 / rows
-    // 2q, 2q+1, packed as two 16-bit lanes.
-    uint32_t xr[ACT == ACT_NONE ? 8 : 1][4];
-    float y[ACT == ACT_NONE ? 1 : 8][8];
-    uint32_t ce[4] = {0u, 0u, 0u, 0u};
-    uint32_t re[4] = {0u, 0u, 0u, 0u};
-    if (ok) {
-      if constexpr (ACT == ACT_NONE) {
+      // ---- load this lane's 8 x 8 block and reduce it to magnitude maxima ---
+      // The plain path keeps the packed bf16 pairs (xr) and widens them where
+      // they are used; the activation paths hold y in fp32.  ce[p] / re[q]:
+      // exponent fields of the largest magnitudes of columns 2p, 2p+1 / rows
+      // 2q, 2q+1, packed as two 16-bit lanes.
+      uint32_t xr[ACT == ACT_NONE ? 8 : 1][4];
+      float y[ACT == ACT_NONE ? 1 : 8][8];
+      uint32_t ce[4] = {0u, 0u, 0u, 0u};
+      uint32_t re[4] = {0u, 0u, 0u, 0u};
+      if (ok) {
+        if constexpr (ACT == ACT_NONE) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = lds128(my_row0 + i * ROW_PITCH);
+            xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
+          }
+          uint32_t cm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            uint32_t tt[2];
+#pragma unroll
+            for (int di = 0; di < 2; ++di) {
+#pragma unroll
+              for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], xr[i + di][p]);
+              tt[di] = absmax_bf16x2(absmax_bf16x2(xr[i + di][0], xr[i + di][1]),
+                                     absmax_bf16x2(xr[i + di][2], xr[i + di][3]));
+            }
+            // low halves: even columns, high halves: odd columns; fold per row.
+            re[i / 2] = bf16_exponents(
+                absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)));
+          }
+#pragma unroll
+          for (int p = 0; p < 4; ++p) ce[p] = bf16_exponents(cm[p]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = lds128(my_row0 + i * ROW_PITCH);
+            uint32_t u[4] = {0u, 0u, 0u, 0u}, w2[4] = {0u, 0u, 0u, 0u};
+            if constexpr (OPERANDS >= 2) {
+              const uint4 w = lds128(my_row0 + L::TILE_BYTES + i * ROW_PITCH);
+              u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w;
+            }
+            if constexpr (OPERANDS >= 3) {
+              const uint4 w = lds128(my_row0 + 2 * L::TILE_BYTES + i * ROW_PITCH);
+              w2[0] = w.x; w2[1] = w.y; w2[2] = w.z; w2[3] = w.w;
+            }
+            const uint32_t g[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              y[i][2 * p] = act_value<ACT>(bf16_lo(g[p]), bf16_lo(u[p]), bf16_lo(w2[p]), t);
+              y[i][2 * p + 1] = act_value<ACT>(bf16_hi(g[p]), bf16_hi(u[p]), bf16_hi(w2[p]), t);
+            }
+          }
+          uint32_t cmx[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          uint32_t rmx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            rmx[i] = 0u;
+#pragma unroll
+            for (int jc = 0; jc < 8; ++jc) {
+              const uint32_t b = __float_as_uint(y[i][jc]) & 0x7FFFFFFFu;
+              cmx[jc] = max(cmx[jc], b);
+              rmx[i] = max(rmx[i], b);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) re[q] = (rmx[2 * q] >> 23) | ((rmx[2 * q + 1] >> 23) << 16);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) ce[p] = (cmx[2 * p] >> 23) | ((cmx[2 * p + 1] >> 23) << 16);
+        }
+      }
+      // Column maxima over the warp's 16 rows, published for the partner warp
+      // that holds the other 16 rows of the same 32-row block.
+#pragma unroll
+      for (int p = 0; p < 4; ++p) ce[p] = vmax_u16x2(ce[p], __shfl_xor_sync(0xFFFFFFFFu, ce[p], 16));
+      const uint32_t xch = sbase + L::OFF_XCH + (warp * 16 + c) * 16;
+      if (COL && h == 0) sts128(xch, ce[0], ce[1], ce[2], ce[3]);
+
+      // ---- barrier A: the slot has been read by every warp, the colwise
+      // staging is free (thread 0 waited for the previous store), the column
+      // maxima are published, and every thread knows whether the copy landed.
+      fence_proxy_async_smem();
+      if (COL && tid == 0) bulk_wait_read<QBUF - 1>();
+      if (__syncthreads_or(!ok)) {
+        // A copy never landed: record it, let the other copies in flight and
+        // the pending stores finish (bounded), and stop without more output.
+        if (tid == 0) {
+          if (a.dev_err) atomicOr(a.dev_err, 1u);
+          for (int jj = j + 1; jj < j + STAGES && jj < count; ++jj)
+            mbar_wait_bounded(bar0 + 8 * (jj % STAGES), (jj / STAGES) & 1, a.timeout_ns);
+          bulk_wait_all();
+        }
+        return;
+      }
+      if (tid == 0 && t == NOUT - 1 && j + STAGES < count) issue_load(j + STAGES);
+
+      // ---- complete the block maxima --------------------------------------
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 1));
+        re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 2));
+      }
+      if constexpr (COL) {
+        const uint4 other = lds128(sbase + L::OFF_XCH + ((warp ^ 1) * 16 + c) * 16);
+        ce[0] = vmax_u16x2(ce[0], other.x);
+        ce[1] = vmax_u16x2(ce[1], other.y);
+        ce[2] = vmax_u16x2(ce[2], other.z);
+        ce[3] = vmax_u16x2(ce[3], other.w);
+      }
+
+      const int col0 = tk * MX_TILE_K + c * 8;            // first column of this lane
+      const bool col_ok = col0 < a.kin;
+      const int obase = t * a.out_half;                   // output column of input column 0
+      const int row0 = band * BAND + 16 * warp + 8 * h;   // first row of this lane
+      const bool row_ok = row0 < a.M;
+      const int slot = tk & 7;                            // rowwise scale gathering slot
+
+      // Values of row i, columns 2p and 2p+1 as an fp32 pair.
+      auto pair_at = [&](int i, int p) -> float2 {
+        if constexpr (ACT == ACT_NONE) {
+          return make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p]));
+        } else {
+          return make_float2(y[i][2 * p], y[i][2 * p + 1]);
+        }
+      };
+
+      // ---- rowwise: codes straight to global, scale bytes to staging --------
+      if constexpr (ROW) {
+        uint32_t rc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) rc[q] = e8m0_pair(re[q]);
+        uint8_t* qrow = a.q_row + static_cast<size_t>(row0) * a.K + obase + col0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = lds128(my_row0 + i * ROW_PITCH);
-          xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
-        }
-        uint32_t cm[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          uint32_t tt[2];
-#pragma unroll
-          for (int di = 0; di < 2; ++di) {
-#pragma unroll
-            for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], xr[i + di][p]);
-            tt[di] = absmax_bf16x2(absmax_bf16x2(xr[i + di][0], xr[i + di][1]),
-                                   absmax_bf16x2(xr[i + di][2], xr[i + di][3]));
-          }
-          // low halves: even columns, high halves: odd columns; fold per row.
-          re[i / 2] = bf16_exponents(
-              absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)));
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) ce[p] = bf16_exponents(cm[p]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = lds128(my_row0 + i * ROW_PITCH);
-          uint32_t u[4] = {0u, 0u, 0u, 0u};
-          if constexpr (ACT == ACT_SWIGLU) {
-            const uint4 w = lds128(my_row0 + L::TILE_BYTES + i * ROW_PITCH);
-            u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w;
-          }
-          const uint32_t g[4] = {v.x, v.y, v.z, v.w};
+          const float inv = inv_scale_from_e8m0(half16(rc[i >> 1], i & 1));
+          const float2 iv = make_float2(inv, inv);
+          uint32_t w[4];
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
-            if constexpr (ACT == ACT_GELU) {
-              y[i][2 * p] = gelu_tanh_f32(bf16_lo(g[p]));
-              y[i][2 * p + 1] = gelu_tanh_f32(bf16_hi(g[p]));
-            } else {
-              y[i][2 * p] = swiglu_f32(bf16_lo(g[p]), bf16_lo(u[p]));
-              y[i][2 * p + 1] = swiglu_f32(bf16_hi(g[p]), bf16_hi(u[p]));
-            }
+            const float2 v = mul_f32x2(pair_at(i, p), iv);
+            w[p] = cvt_e4m3x2(v.x, v.y);
           }
+          if (col_ok && row_ok)
+            stg64_cs(qrow + static_cast<size_t>(i) * a.K, w[0] | (w[1] << 16), w[2] | (w[3] << 16));
         }
-        uint32_t cmx[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        uint32_t rmx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          rmx[i] = 0u;
-#pragma unroll
-          for (int jc = 0; jc < 8; ++jc) {
-            const uint32_t b = __float_as_uint(y[i][jc]) & 0x7FFFFFFFu;
-            cmx[jc] = max(cmx[jc], b);
-            rmx[i] = max(rmx[i], b);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) re[q] = (rmx[2 * q] >> 23) | ((rmx[2 * q + 1] >> 23) << 16);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) ce[p] = (cmx[2 * p] >> 23) | ((cmx[2 * p + 1] >> 23) << 16);
+        // Lane (h, c) holds block c/4's codes for its 8 rows; it stages rows
+        // r and r + 4 (r = c & 3) into [BAND rows][8 slots][4 blocks].
+        const int r = c & 3, b = c >> 2;
+        const uint32_t rs =
+            sbase + L::OFF_RSC + ((t * GROUP + pos.bi) * BAND + 16 * warp + 8 * h + r) * 32 +
+            slot * 4 + b;
+        const int sh = 16 * (r & 1);
+        sts8(rs, ((r >> 1 ? rc[1] : rc[0]) >> sh) & 0xFFu);
+        sts8(rs + 4 * 32, ((r >> 1 ? rc[3] : rc[2]) >> sh) & 0xFFu);
       }
-    }
-    // Column maxima over the warp's 16 rows, published for the partner warp
-    // that holds the other 16 rows of the same 32-row block.
+
+      // ---- colwise: codes and scale bytes to staging -------------------------
+      if constexpr (COL) {
+        uint32_t cc[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) ce[p] = vmax_u16x2(ce[p], __shfl_xor_sync(0xFFFFFFFFu, ce[p], 16));
-    const uint32_t xch = sbase + L::OFF_XCH + (warp * 16 + c) * 16;
-    if (COL && h == 0) sts128(xch, ce[0], ce[1], ce[2], ce[3]);
-
-    // ---- barrier A: the slot has been read by every warp, the colwise
-    // staging is free (thread 0 waited for the previous store), the column
-    // maxima are published, and every thread knows whether the copy landed.
-    fence_proxy_async_smem();
-    if (COL && tid == 0) bulk_wait_read<QBUF - 1>();
-    if (__syncthreads_or(!ok)) {
-      // A copy never landed: record it, let the other copies in flight and
-      // the pending stores finish (bounded), and stop without more output.
-      if (tid == 0) {
-        if (a.dev_err) atomicOr(a.dev_err, 1u);
-        for (int jj = j + 1; jj < j + STAGES && jj < count; ++jj)
-          mbar_wait_bounded(bar0 + 8 * (jj % STAGES), (jj / STAGES) & 1, a.timeout_ns);
-        bulk_wait_all();
-      }
-      return;
-    }
-    if (tid == 0 && j + STAGES < count) issue_load(j + STAGES);
-
-    // ---- complete the block maxima --------------------------------------
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 1));
-      re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 2));
-    }
-    if constexpr (COL) {
-      const uint4 other = lds128(sbase + L::OFF_XCH + ((warp ^ 1) * 16 + c) * 16);
-      ce[0] = vmax_u16x2(ce[0], other.x);
-      ce[1] = vmax_u16x2(ce[1], other.y);
-      ce[2] = vmax_u16x2(ce[2], other.z);
-      ce[3] = vmax_u16x2(ce[3], other.w);
-    }
-
-    const int col0 = tk * MX_TILE_K + c * 8;            // first column of this lane
-    const bool col_ok = col0 < a.K;
-    const int row0 = band * BAND + 16 * warp + 8 * h;   // first row of this lane
-    const bool row_ok = row0 < a.M;
-    const int slot = tk & 7;                            // rowwise scale gathering slot
-
-    // Values of row i, columns 2p and 2p+1 as an fp32 pair.
-    auto pair_at = [&](int i, int p) -> float2 {
-      if constexpr (ACT == ACT_NONE) {
-        return make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p]));
-      } else {
-        return make_float2(y[i][2 * p], y[i][2 * p + 1]);
-      }
-    };
-
-    // ---- rowwise: codes straight to global, scale bytes to staging --------
-    if constexpr (ROW) {
-      uint32_t rc[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) rc[q] = e8m0_pair(re[q]);
-      uint8_t* qrow = a.q_row + static_cast<size_t>(row0) * a.K + col0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float inv = inv_scale_from_e8m0(half16(rc[i >> 1], i & 1));
-        const float2 iv = make_float2(inv, inv);
-        uint32_t w[4];
+        for (int p = 0; p < 4; ++p) cc[p] = e8m0_pair(ce[p]);
+        // Staging half (warp / 8) holds m = 128 * half + 0..127 as
+        // [k % 8][k / 8][128 m], the 16-byte chunk index xor-ed with (k / 8) % 8
+        // (the 128-byte swizzle of the store's tensor map).  The lane's 8 rows
+        // are the h-th 8-byte half of chunk (warp % 8).
+        const uint32_t qs = sbase + L::OFF_QCOL + (j % QBUF) * L::QCOL_BUF +
+                            (warp >> 3) * L::QCOL_HALF + c * 128 +
+                            (((warp & 7) ^ (c & 7)) << 4) + 8 * h;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          const float2 v = mul_f32x2(pair_at(i, p), iv);
-          w[p] = cvt_e4m3x2(v.x, v.y);
-        }
-        if (col_ok && row_ok)
-          stg64_cs(qrow + static_cast<size_t>(i) * a.K, w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-      }
-      // Lane (h, c) holds block c/4's codes for its 8 rows; it stages rows
-      // r and r + 4 (r = c & 3) into [BAND rows][8 slots][4 blocks].
-      const int r = c & 3, b = c >> 2;
-      const uint32_t rs =
-          sbase + L::OFF_RSC + (pos.bi * BAND + 16 * warp + 8 * h + r) * 32 + slot * 4 + b;
-      const int sh = 16 * (r & 1);
-      sts8(rs, ((r >> 1 ? rc[1] : rc[0]) >> sh) & 0xFFu);
-      sts8(rs + 4 * 32, ((r >> 1 ? rc[3] : rc[2]) >> sh) & 0xFFu);
-    }
-
-    // ---- colwise: codes and scale bytes to staging -------------------------
-    if constexpr (COL) {
-      uint32_t cc[4];
+          const float2 iv = make_float2(inv_scale_from_e8m0(half16(cc[p], 0)),
+                                        inv_scale_from_e8m0(half16(cc[p], 1)));
+          uint32_t we[4], wo[4];   // codes of columns 2p (even) and 2p+1 (odd), two rows each
 #pragma unroll
-      for (int p = 0; p < 4; ++p) cc[p] = e8m0_pair(ce[p]);
-      // Staging half (warp / 8) holds m = 128 * half + 0..127 as
-      // [k % 8][k / 8][128 m], the 16-byte chunk index xor-ed with (k / 8) % 8
-      // (the 128-byte swizzle of the store's tensor map).  The lane's 8 rows
-      // are the h-th 8-byte half of chunk (warp % 8).
-      const uint32_t qs = sbase + L::OFF_QCOL + (j % QBUF) * L::QCOL_BUF +
-                          (warp >> 3) * L::QCOL_HALF + c * 128 +
-                          (((warp & 7) ^ (c & 7)) << 4) + 8 * h;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float2 iv = make_float2(inv_scale_from_e8m0(half16(cc[p], 0)),
-                                      inv_scale_from_e8m0(half16(cc[p], 1)));
-        uint32_t we[4], wo[4];   // codes of columns 2p (even) and 2p+1 (odd), two rows each
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const float2 r0 = mul_f32x2(pair_at(i, p), iv);
-          const float2 r1 = mul_f32x2(pair_at(i + 1, p), iv);
-          we[i / 2] = cvt_e4m3x2(r0.x, r1.x);
-          wo[i / 2] = cvt_e4m3x2(r0.y, r1.y);
-        }
-        sts64(qs + (2 * p) * 2048, we[0] | (we[1] << 16), we[2] | (we[3] << 16));
-        sts64(qs + (2 * p + 1) * 2048, wo[0] | (wo[1] << 16), wo[2] | (wo[3] << 16));
-      }
-      // Scale bytes of block (band bi, warp / 2); both warps of a block hold
-      // the same codes, the even one writes them (h = 0: columns 0-3, h = 1:
-      // columns 4-7 of the lane's chunk).
-      if ((warp & 1) == 0) {
-        const int blk = pos.bi * L::BPB + (warp >> 1);
-        if constexpr (L::CSC_BY_COL) {
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
-            sts8(sbase + L::OFF_CSC + L::csc(blk, c * 8 + 4 * h + jj),
-                 (pair >> (16 * (jj & 1))) & 0xFFu);
+          for (int i = 0; i < 8; i += 2) {
+            const float2 r0 = mul_f32x2(pair_at(i, p), iv);
+            const float2 r1 = mul_f32x2(pair_at(i + 1, p), iv);
+            we[i / 2] = cvt_e4m3x2(r0.x, r1.x);
+            wo[i / 2] = cvt_e4m3x2(r0.y, r1.y);
           }
-        } else {
-          sts32(sbase + L::OFF_CSC + L::csc(blk, c * 8 + 4 * h),
-                h ? prmt(cc[2], cc[3], 0x6420) : prmt(cc[0], cc[1], 0x6420));
+          sts64(qs + (2 * p) * 2048, we[0] | (we[1] << 16), we[2] | (we[3] << 16));
+          sts64(qs + (2 * p + 1) * 2048, wo[0] | (wo[1] << 16), wo[2] | (wo[3] << 16));
         }
-      }
-    }
-
-    // ---- dbias: column sums of the warp's 16 rows, pairwise ----------------
-    if constexpr (DBIAS) {
+        // Scale bytes of block (band bi, warp / 2); both warps of a block hold
+        // the same codes, the even one writes them (h = 0: columns 0-3, h = 1:
+        // columns 4-7 of the lane's chunk).
+        if ((warp & 1) == 0) {
+          const int blk = pos.bi * L::BPB + (warp >> 1);
+          if constexpr (L::CSC_BY_COL) {
 #pragma unroll
-      for (int jc = 0; jc < 8; ++jc) {
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 pr = pair_at(i, jc >> 1);
-          v[i] = (jc & 1) ? pr.y : pr.x;
-        }
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
-        const float s16 = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
-        if (h == 0) {
-          float* db = reinterpret_cast<float*>(smem + L::OFF_DB) + warp * MX_TILE_K + c * 8 + jc;
-          *db = s16;
-        }
-      }
-    }
-
-    // ---- barrier B: the band's staging is complete -------------------------
-    fence_proxy_async_smem();
-    bar_sync_cta(THREADS);
-
-    if constexpr (COL) {
-      if (tid == 0) {
-#pragma unroll
-        for (int half = 0; half < L::QCOL_HALVES; ++half)
-          tma_store_3d(&tmap_qcol,
-                       sbase + L::OFF_QCOL + (j % QBUF) * L::QCOL_BUF + half * L::QCOL_HALF,
-                       band * BAND + 128 * half, tk * (MX_TILE_K / 8), 0);
-        bulk_commit();
-      }
-      // Colwise scale bytes, once the group's last band (or this CTA's last
-      // step) is staged: one run of up to GROUP * BAND / 32 blocks per column.
-      if (pos.bi + 1 == pos.nb || j + 1 == count) {
-        constexpr int NB = GROUP * L::BPB;
-        constexpr int CH = NB < 16 ? NB : 16;               // bytes per store
-        const int fb = (pos.g == p0.g && tk == p0.tk) ? p0.bi : 0;   // first band staged
-        const int mb0 = (pos.g * GROUP + fb) * L::BPB;     // its first block along m
-        const int nblk = min((pos.bi + 1 - fb) * L::BPB, nmb - mb0);
-        if (nblk == NB && (nmb % CH) == 0) {
-          // Item i = (chunk, column); warp w takes items w * IPW .. + IPW - 1.
-          constexpr int ITEMS = MX_TILE_K * (NB / CH);
-          constexpr int IPW = ITEMS / WARPS;
-          static_assert(ITEMS % WARPS == 0 && IPW <= 32, "one item per lane");
-          if (lane < IPW) {
-            const int i = warp * IPW + lane;
-            const int kc = i % MX_TILE_K, ch = i / MX_TILE_K;
-            const int k = tk * MX_TILE_K + kc;
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            if constexpr (L::CSC_BY_COL) {
-              w[0] = lds32(sbase + L::OFF_CSC + L::csc(0, kc));
-            } else {
-#pragma unroll
-              for (int bb = 0; bb < CH; ++bb)
-                w[bb >> 2] |= ld_shared_u8(sbase + L::OFF_CSC + L::csc(ch * CH + bb, kc))
-                              << (8 * (bb & 3));
+            for (int jj = 0; jj < 4; ++jj) {
+              const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
+              sts8(sbase + L::OFF_CSC + L::csc(blk, c * 8 + 4 * h + jj),
+                   (pair >> (16 * (jj & 1))) & 0xFFu);
             }
-            uint8_t* dst = a.s_col + static_cast<size_t>(k) * nmb + mb0 + ch * CH;
-            if (k < a.K) {
-              if (CH == 16) stg128(dst, w[0], w[1], w[2], w[3]);
-              else if (CH == 8) stg64(dst, w[0], w[1]);
-              else stg32(dst, w[0]);
-            }
-          }
-        } else {
-          for (int kc = tid; kc < MX_TILE_K; kc += THREADS) {
-            const int k = tk * MX_TILE_K + kc;
-            if (k >= a.K) continue;
-            uint8_t* dst = a.s_col + static_cast<size_t>(k) * nmb + mb0;
-            for (int bb = 0; bb < nblk; ++bb)
-              stg8(dst + bb, ld_shared_u8(sbase + L::OFF_CSC + L::csc(fb * L::BPB + bb, kc)));
-          }
-        }
-      }
-    }
-
-    if constexpr (ROW) {
-      // This band's next step in this CTA, if any, is j + nb.
-      const bool flush = (slot == 7) || (tk + 1 == a.tiles_k) || (j + pos.nb >= count);
-      if (flush) {
-        // Rowwise scale bytes of steps rsc_first..slot of this group of eight
-        // (the CTA's first step for this band may fall inside the group):
-        // one 32-byte sector per row when all eight steps are present.  Warp
-        // w writes the 16 rows it quantized.
-        const int first_tk = (pos.g == p0.g) ? p0.tk + (pos.bi < p0.bi ? 1 : 0) : 0;
-        const int rsc_first = first_tk > (tk & ~7) ? (first_tk & 7) : 0;
-        const int rr = 16 * warp + lane;
-        const int row = band * BAND + rr;
-        if (lane < 16 && row < a.M) {
-          const int kb0 = (tk - slot) * 4;   // first k-block of the group
-          uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
-          const uint32_t src = sbase + L::OFF_RSC + (pos.bi * BAND + rr) * 32;
-          // Two 16-byte stores: every row start must be 16-byte aligned.
-          if (rsc_first == 0 && slot == 7 && (nkb & 15) == 0) {
-            const uint4 lo = lds128(src), hi = lds128(src + 16);
-            stg128(dst, lo.x, lo.y, lo.z, lo.w);
-            stg128(dst + 16, hi.x, hi.y, hi.z, hi.w);
           } else {
-            const int b_end = min((slot + 1) * 4, nkb - kb0);
-            for (int bb = rsc_first * 4; bb < b_end; ++bb)
-              stg8(dst + bb, (lds32(src + (bb & ~3)) >> (8 * (bb & 3))) & 0xFFu);
+            sts32(sbase + L::OFF_CSC + L::csc(blk, c * 8 + 4 * h),
+                  h ? prmt(cc[2], cc[3], 0x6420) : prmt(cc[0], cc[1], 0x6420));
           }
         }
       }
-    }
 
-    if constexpr (DBIAS) {
-      // The band's sum of each column: pairwise over the warps' 16-row sums;
-      // warp w adds up 128 / WARPS columns.
-      constexpr int COLS_PER_WARP = MX_TILE_K / WARPS;
-      if (lane < COLS_PER_WARP) {
-        const int kc = warp * COLS_PER_WARP + lane;
-        const int k = tk * MX_TILE_K + kc;
-        const float* db = reinterpret_cast<const float*>(smem + L::OFF_DB) + kc;
-        float v[WARPS];
+      // ---- dbias: column sums of the warp's 16 rows, pairwise ----------------
+      if constexpr (DBIAS) {
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) v[w] = db[w * MX_TILE_K];
+        for (int jc = 0; jc < 8; ++jc) {
+          float v[8];
 #pragma unroll
-        for (int w = WARPS / 2; w >= 1; w >>= 1)
+          for (int i = 0; i < 8; ++i) {
+            const float2 pr = pair_at(i, jc >> 1);
+            v[i] = (jc & 1) ? pr.y : pr.x;
+          }
 #pragma unroll
-          for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
-        if (k < a.K) a.dbias_ws[static_cast<size_t>(band) * a.K + k] = v[0];
+          for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
+          const float s16 = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
+          if (h == 0) {
+            float* db = reinterpret_cast<float*>(smem + L::OFF_DB) + warp * MX_TILE_K + c * 8 + jc;
+            *db = s16;
+          }
+        }
+      }
+
+      // ---- barrier B: the band's staging is complete -------------------------
+      fence_proxy_async_smem();
+      bar_sync_cta(THREADS);
+
+      if constexpr (COL) {
+        if (tid == 0) {
+#pragma unroll
+          for (int half = 0; half < L::QCOL_HALVES; ++half)
+            tma_store_3d(t == 0 ? &tmap_qcol : &tmap_qcol2,
+                         sbase + L::OFF_QCOL + (j % QBUF) * L::QCOL_BUF + half * L::QCOL_HALF,
+                         band * BAND + 128 * half, tk * (MX_TILE_K / 8), 0);
+          bulk_commit();
+        }
+        // Colwise scale bytes, once the group's last band (or this CTA's last
+        // step) is staged: one run of up to GROUP * BAND / 32 blocks per column.
+        if (pos.bi + 1 == pos.nb || j + 1 == count) {
+          constexpr int NB = GROUP * L::BPB;
+          constexpr int CH = NB < 16 ? NB : 16;               // bytes per store
+          const int fb = (pos.g == p0.g && tk == p0.tk) ? p0.bi : 0;   // first band staged
+          const int mb0 = (pos.g * GROUP + fb) * L::BPB;     // its first block along m
+          const int nblk = min((pos.bi + 1 - fb) * L::BPB, nmb - mb0);
+          if (nblk == NB && (nmb % CH) == 0) {
+            // Item i = (chunk, column); warp w takes items w * IPW .. + IPW - 1.
+            constexpr int ITEMS = MX_TILE_K * (NB / CH);
+            constexpr int IPW = ITEMS / WARPS;
+            static_assert(ITEMS % WARPS == 0 && IPW <= 32, "one item per lane");
+            if (lane < IPW) {
+              const int i = warp * IPW + lane;
+              const int kc = i % MX_TILE_K, ch = i / MX_TILE_K;
+              const int k = tk * MX_TILE_K + kc;
+              uint32_t w[4] = {0u, 0u, 0u, 0u};
+              if constexpr (L::CSC_BY_COL) {
+                w[0] = lds32(sbase + L::OFF_CSC + L::csc(0, kc));
+              } else {
+#pragma unroll
+                for (int bb = 0; bb < CH; ++bb)
+                  w[bb >> 2] |= ld_shared_u8(sbase + L::OFF_CSC + L::csc(ch * CH + bb, kc))
+                                << (8 * (bb & 3));
+              }
+              uint8_t* dst = a.s_col + static_cast<size_t>(obase + k) * nmb + mb0 + ch * CH;
+              if (k < a.kin) {
+                if (CH == 16) stg128(dst, w[0], w[1], w[2], w[3]);
+                else if (CH == 8) stg64(dst, w[0], w[1]);
+                else stg32(dst, w[0]);
+              }
+            }
+          } else {
+            for (int kc = tid; kc < MX_TILE_K; kc += THREADS) {
+              const int k = tk * MX_TILE_K + kc;
+              if (k >= a.kin) continue;
+              uint8_t* dst = a.s_col + static_cast<size_t>(obase + k) * nmb + mb0;
+              for (int bb = 0; bb < nblk; ++bb)
+                stg8(dst + bb, ld_shared_u8(sbase + L::OFF_CSC + L::csc(fb * L::BPB + bb, kc)));
+            }
+          }
+        }
+      }
+
+      if constexpr (ROW) {
+        // This band's next step in this CTA, if any, is j + nb.
+        const bool flush = (slot == 7) || (tk + 1 == a.tiles_k) || (j + pos.nb >= count);
+        if (flush) {
+          // Rowwise scale bytes of steps rsc_first..slot of this group of eight
+          // (the CTA's first step for this band may fall inside the group):
+          // one 32-byte sector per row when all eight steps are present.  Warp
+          // w writes the 16 rows it quantized.
+          const int first_tk = (pos.g == p0.g) ? p0.tk + (pos.bi < p0.bi ? 1 : 0) : 0;
+          const int rsc_first = first_tk > (tk & ~7) ? (first_tk & 7) : 0;
+          const int rr = 16 * warp + lane;
+          const int row = band * BAND + rr;
+          if (lane < 16 && row < a.M) {
+            const int kb0 = (tk - slot) * 4;   // first k-block of the group
+            uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + (obase >> 5) + kb0;
+            const uint32_t src = sbase + L::OFF_RSC + ((t * GROUP + pos.bi) * BAND + rr) * 32;
+            // Two 16-byte stores: every row start must be 16-byte aligned.
+            if (rsc_first == 0 && slot == 7 && ((nkb | (obase >> 5)) & 15) == 0) {
+              const uint4 lo = lds128(src), hi = lds128(src + 16);
+              stg128(dst, lo.x, lo.y, lo.z, lo.w);
+              stg128(dst + 16, hi.x, hi.y, hi.z, hi.w);
+            } else {
+              const int b_end = min((slot + 1) * 4, (a.kin >> 5) - kb0);
+              for (int bb = rsc_first * 4; bb < b_end; ++bb)
+                stg8(dst + bb, (lds32(src + (bb & ~3)) >> (8 * (bb & 3))) & 0xFFu);
+            }
+          }
+        }
+      }
+
+      if constexpr (DBIAS) {
+        // The band's sum of each column: pairwise over the warps' 16-row sums;
+        // warp w adds up 128 / WARPS columns.
+        constexpr int COLS_PER_WARP = MX_TILE_K / WARPS;
+        if (lane < COLS_PER_WARP) {
+          const int kc = warp * COLS_PER_WARP + lane;
+          const int k = tk * MX_TILE_K + kc;
+          const float* db = reinterpret_cast<const float*>(smem + L::OFF_DB) + kc;
+          float v[WARPS];
+#pragma unroll
+          for (int w = 0; w < WARPS; ++w) v[w] = db[w * MX_TILE_K];
+#pragma unroll
+          for (int w = WARPS / 2; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
+          if (k < a.kin) a.dbias_ws[static_cast<size_t>(band) * a.K + k] = v[0];
+        }
       }
     }
   }
@@ -664,6 +743,27 @@ struct MxConfig<ACT_SWIGLU> {   // gate + up per slot
   static constexpr int GROUP_COL = MXQ_SWIGLU_GROUP_COL;  // colwise only
   static constexpr int QBUF = MXQ_SWIGLU_QBUF;            // colwise staging buffers
 };
+// The other two-operand paths (GeGLU; grad + x of the backward fusions)
+// share the SwiGLU configuration.
+template <>
+struct MxConfig<ACT_GEGLU> : MxConfig<ACT_SWIGLU> {};
+template <>
+struct MxConfig<ACT_DGELU> : MxConfig<ACT_SWIGLU> {};
+template <>
+struct MxConfig<ACT_DSILU> : MxConfig<ACT_SWIGLU> {};
+// Gated backward: grad, gate and up per slot (96 KiB), two slots, one band
+// per CTA (two outputs per step).
+struct MxConfigDGated {
+  static constexpr int WARPS = 8;
+  static constexpr int STAGES = 2;
+  static constexpr int GROUP = 1;
+  static constexpr int GROUP_COL = 1;
+  static constexpr int QBUF = 1;
+};
+template <>
+struct MxConfig<ACT_DSWIGLU> : MxConfigDGated {};
+template <>
+struct MxConfig<ACT_DGEGLU> : MxConfigDGated {};
 
 template <int MODE, bool DBIAS, int ACT>
 cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
@@ -678,7 +778,8 @@ cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
   // pitch changes how the warps' store phases line up; measured on GB300,
   // 8 bytes is faster for the plain cast and 4 bytes for the fused paths.
   constexpr int CPITCH = (ACT == ACT_NONE && !DBIAS) ? 8 : 4;
-  using L = MxLayout<WARPS, ACT == ACT_SWIGLU ? 2 : 1, STAGES, GROUP, QBUF, CPITCH>;
+  using L = MxLayout<WARPS, act_operands(ACT), STAGES, GROUP, QBUF, CPITCH, act_outputs(ACT)>;
+  static_assert(L::DYNAMIC <= 227 * 1024, "shared memory per CTA");
   auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS, STAGES, GROUP, QBUF, CPITCH>;
 
   static int configured_device = -1;
@@ -692,7 +793,8 @@ cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
   }
   const int64_t steps = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
   const int grid = static_cast<int>(steps < num_sms ? steps : num_sms);
-  kernel<<<grid < 1 ? 1 : grid, WARPS * 32, L::DYNAMIC, stream>>>(maps.x, maps.q_col, a);
+  kernel<<<grid < 1 ? 1 : grid, WARPS * 32, L::DYNAMIC, stream>>>(maps.x, maps.x2, maps.q_col,
+                                                                   maps.q_col2, a);
   return cudaGetLastError();
 }
 
@@ -712,16 +814,32 @@ int mx_band_rows(int act) {
   switch (act) {
     case ACT_GELU: return 16 * MxConfig<ACT_GELU>::WARPS;
     case ACT_SWIGLU: return 16 * MxConfig<ACT_SWIGLU>::WARPS;
+    case ACT_GEGLU: return 16 * MxConfig<ACT_GEGLU>::WARPS;
+    case ACT_DGELU: return 16 * MxConfig<ACT_DGELU>::WARPS;
+    case ACT_DSILU: return 16 * MxConfig<ACT_DSILU>::WARPS;
+    case ACT_DSWIGLU: return 16 * MxConfig<ACT_DSWIGLU>::WARPS;
+    case ACT_DGEGLU: return 16 * MxConfig<ACT_DGEGLU>::WARPS;
     default: return 16 * MxConfig<ACT_NONE>::WARPS;
   }
 }
 
 cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
                       int num_sms, cudaStream_t stream) {
-  if (dbias) return launch_mode<true, ACT_NONE>(maps, a, mode, num_sms, stream);
+  if (dbias) {
+    switch (act) {
+      case ACT_DGELU: return launch_mode<true, ACT_DGELU>(maps, a, mode, num_sms, stream);
+      case ACT_DSILU: return launch_mode<true, ACT_DSILU>(maps, a, mode, num_sms, stream);
+      default: return launch_mode<true, ACT_NONE>(maps, a, mode, num_sms, stream);
+    }
+  }
   switch (act) {
     case ACT_GELU: return launch_mode<false, ACT_GELU>(maps, a, mode, num_sms, stream);
     case ACT_SWIGLU: return launch_mode<false, ACT_SWIGLU>(maps, a, mode, num_sms, stream);
+    case ACT_GEGLU: return launch_mode<false, ACT_GEGLU>(maps, a, mode, num_sms, stream);
+    case ACT_DGELU: return launch_mode<false, ACT_DGELU>(maps, a, mode, num_sms, stream);
+    case ACT_DSILU: return launch_mode<false, ACT_DSILU>(maps, a, mode, num_sms, stream);
+    case ACT_DSWIGLU: return launch_mode<false, ACT_DSWIGLU>(maps, a, mode, num_sms, stream);
+    case ACT_DGEGLU: return launch_mode<false, ACT_DGEGLU>(maps, a, mode, num_sms, stream);
     default: return launch_mode<false, ACT_NONE>(maps, a, mode, num_sms, stream);
   }
 }

@@ -159,8 +159,8 @@ const char* mxq_status_string(int status) {
 size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags) {
   if (M <= 0 || K <= 0) return 0;
   if (op == MXQ_OP_NVFP4) return 16;   // one fp32 amax, padded
-  if (op != MXQ_OP_ROWCOL || !(flags & MXQ_DBIAS)) return 0;
-  const int64_t band = mxq::mx_band_rows(mxq::ACT_NONE);
+  if ((op != MXQ_OP_ROWCOL && op != MXQ_OP_DACT) || !(flags & MXQ_DBIAS)) return 0;
+  const int64_t band = mxq::mx_band_rows(op == MXQ_OP_DACT ? mxq::ACT_DGELU : mxq::ACT_NONE);
   const int64_t bands = (M + band - 1) / band;
   return static_cast<size_t>(bands) * static_cast<size_t>(K) * sizeof(float);
 }
@@ -199,6 +199,7 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.tiles_m = static_cast<int>((M + band - 1) / band);
+  a.kin = static_cast<int>(K);
   a.tiles_k = static_cast<int>((K + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
   a.q_row = q_row;
   a.s_row = s_row;
@@ -215,10 +216,12 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   mxq::MxMaps maps{};
   st = encode_bf16_map(&maps.x, x, M, K, ldx, mxq::MX_TILE_K, band);
   if (st != MXQ_OK) return st;
+  maps.x2 = maps.x;
   if (flags & MXQ_COLWISE) {
     st = encode_mx_qcol_map(&maps.q_col, M, K, q_col);
     if (st != MXQ_OK) return st;
   }
+  maps.q_col2 = maps.q_col;
   st = from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
   if (st != MXQ_OK || !want_dbias) return st;
   return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
@@ -227,8 +230,10 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
 mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, uint32_t flags,
                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                              uint32_t* dev_err, mxq_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE)) return MXQ_EINVAL;
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU))
+    return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
+  if ((flags & MXQ_ACT_GELU_TANH) && (flags & MXQ_ACT_SILU)) return MXQ_EINVAL;
   if (M < 0 || N < 0 || ldx < 2 * N) return MXQ_ESHAPE;
   if ((M % 32) || (N % 32)) return MXQ_ESHAPE;
   if (M > (int64_t(1) << 30) || N > (int64_t(1) << 29) || M * N > (int64_t(1) << 40))
@@ -242,10 +247,12 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
   st = check_mx_outputs(flags, N, q_row, s_row, q_col, s_col);
   if (st != MXQ_OK) return st;
 
-  const int band = mxq::mx_band_rows(mxq::ACT_SWIGLU);
+  const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_GEGLU : mxq::ACT_SWIGLU;
+  const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(N);
+  a.kin = static_cast<int>(N);
   a.tiles_m = static_cast<int>((M + band - 1) / band);
   a.tiles_k = static_cast<int>((N + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
   a.up_col = static_cast<int>(N);
@@ -260,11 +267,131 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
   // at N + k.
   st = encode_bf16_map(&maps.x, x, M, 2 * N, ldx, mxq::MX_TILE_K, band);
   if (st != MXQ_OK) return st;
+  maps.x2 = maps.x;
   if (flags & MXQ_COLWISE) {
     st = encode_mx_qcol_map(&maps.q_col, M, N, q_col);
     if (st != MXQ_OK) return st;
   }
-  return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, mxq::ACT_SWIGLU, sms, stream));
+  maps.q_col2 = maps.q_col;
+  return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, act, sms, stream));
+}
+
+mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t K, int64_t ldg,
+                            int64_t ldx, uint32_t flags, uint8_t* q_row, uint8_t* s_row,
+                            uint8_t* q_col, uint8_t* s_col, float* dbias, void* workspace,
+                            size_t workspace_bytes, uint32_t* dev_err, mxq_stream_t stream) {
+  const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU;
+  if (flags & ~known) return MXQ_EINVAL;
+  if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
+  const bool gelu = (flags & MXQ_ACT_GELU_TANH) != 0, silu = (flags & MXQ_ACT_SILU) != 0;
+  if (gelu == silu) return MXQ_EINVAL;   // exactly one activation
+  if (M < 0 || K < 0 || ldg < K || ldx < K) return MXQ_ESHAPE;
+  if ((M % 32) || (K % 32)) return MXQ_ESHAPE;
+  if (M > (int64_t(1) << 30) || K > (int64_t(1) << 30) || M * K > (int64_t(1) << 40))
+    return MXQ_ESHAPE;
+  const bool want_dbias = (flags & MXQ_DBIAS) != 0;
+  if (want_dbias && !dbias) return MXQ_EINVAL;
+  if (want_dbias && !aligned(dbias, 16)) return MXQ_EALIGN;
+  int sms = 0;
+  mxq_status st = current_device(&sms);
+  if (st != MXQ_OK) return st;
+  if (M == 0 || K == 0) {
+    if (want_dbias && K > 0)
+      return from_cuda(cudaMemsetAsync(dbias, 0, static_cast<size_t>(K) * sizeof(float), stream));
+    return MXQ_OK;
+  }
+  if (!grad || !x) return MXQ_EINVAL;
+  if (!aligned(grad, 16) || !aligned(x, 16) || (ldg % 8) || (ldx % 8)) return MXQ_EALIGN;
+  st = check_mx_outputs(flags, K, q_row, s_row, q_col, s_col);
+  if (st != MXQ_OK) return st;
+
+  const int act = gelu ? mxq::ACT_DGELU : mxq::ACT_DSILU;
+  const int band = mxq::mx_band_rows(act);
+  mxq::MxArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.kin = static_cast<int>(K);
+  a.tiles_m = static_cast<int>((M + band - 1) / band);
+  a.tiles_k = static_cast<int>((K + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_col = q_col;
+  a.s_col = s_col;
+  a.dev_err = dev_err;
+  a.timeout_ns = DEFAULT_TIMEOUT_NS;
+  if (want_dbias) {
+    const size_t need = static_cast<size_t>(a.tiles_m) * static_cast<size_t>(K) * sizeof(float);
+    if (!workspace || workspace_bytes < need) return MXQ_EWORKSPACE;
+    if (!aligned(workspace, 16)) return MXQ_EALIGN;
+    a.dbias_ws = static_cast<float*>(workspace);
+  }
+  mxq::MxMaps maps{};
+  st = encode_bf16_map(&maps.x, grad, M, K, ldg, mxq::MX_TILE_K, band);
+  if (st != MXQ_OK) return st;
+  st = encode_bf16_map(&maps.x2, x, M, K, ldx, mxq::MX_TILE_K, band);
+  if (st != MXQ_OK) return st;
+  if (flags & MXQ_COLWISE) {
+    st = encode_mx_qcol_map(&maps.q_col, M, K, q_col);
+    if (st != MXQ_OK) return st;
+  }
+  maps.q_col2 = maps.q_col;
+  st = from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
+  if (st != MXQ_OK || !want_dbias) return st;
+  return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
+}
+
+mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_t N, int64_t ldg,
+                              int64_t ldx, uint32_t flags, uint8_t* q_row, uint8_t* s_row,
+                              uint8_t* q_col, uint8_t* s_col, uint32_t* dev_err,
+                              mxq_stream_t stream) {
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU))
+    return MXQ_EINVAL;
+  if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
+  if ((flags & MXQ_ACT_GELU_TANH) && (flags & MXQ_ACT_SILU)) return MXQ_EINVAL;
+  if (M < 0 || N < 0 || ldg < N || ldx < 2 * N) return MXQ_ESHAPE;
+  if ((M % 32) || (N % 32)) return MXQ_ESHAPE;
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 29) || M * N > (int64_t(1) << 39))
+    return MXQ_ESHAPE;
+  int sms = 0;
+  mxq_status st = current_device(&sms);
+  if (st != MXQ_OK) return st;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!grad || !x) return MXQ_EINVAL;
+  if (!aligned(grad, 16) || !aligned(x, 16) || (ldg % 8) || (ldx % 8)) return MXQ_EALIGN;
+  st = check_mx_outputs(flags, 2 * N, q_row, s_row, q_col, s_col);
+  if (st != MXQ_OK) return st;
+
+  const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_DGEGLU : mxq::ACT_DSWIGLU;
+  const int band = mxq::mx_band_rows(act);
+  mxq::MxArgs a{};
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(2 * N);       // output width
+  a.kin = static_cast<int>(N);
+  a.out_half = static_cast<int>(N);    // d up starts at output column N
+  a.tiles_m = static_cast<int>((M + band - 1) / band);
+  a.tiles_k = static_cast<int>((N + mxq::MX_TILE_K - 1) / mxq::MX_TILE_K);
+  a.up_col = 0;                        // gate: columns 0.. of x
+  a.up_col2 = static_cast<int>(N);     // up: columns N.. of x
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.q_col = q_col;
+  a.s_col = s_col;
+  a.dev_err = dev_err;
+  a.timeout_ns = DEFAULT_TIMEOUT_NS;
+  mxq::MxMaps maps{};
+  st = encode_bf16_map(&maps.x, grad, M, N, ldg, mxq::MX_TILE_K, band);
+  if (st != MXQ_OK) return st;
+  st = encode_bf16_map(&maps.x2, x, M, 2 * N, ldx, mxq::MX_TILE_K, band);
+  if (st != MXQ_OK) return st;
+  if (flags & MXQ_COLWISE) {
+    // One map per output tile, each clipped at its N code rows, so a ragged
+    // last tile of d gate cannot spill into the rows of d up.
+    st = encode_mx_qcol_map(&maps.q_col, M, N, q_col);
+    if (st != MXQ_OK) return st;
+    st = encode_mx_qcol_map(&maps.q_col2, M, N, q_col + static_cast<size_t>(N) * M);
+    if (st != MXQ_OK) return st;
+  }
+  return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, act, sms, stream));
 }
 
 mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* amax_out,

@@ -18,12 +18,21 @@ constexpr int MX_TILE_K = 128;
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000000000ull;   // 1 s per wait
 
 enum : int { MX_ROW = 1, MX_COL = 2 };
-enum : int { ACT_NONE = 0, ACT_GELU = 1, ACT_SWIGLU = 2 };
+// Element functions of the MXFP8 kernel: the input itself, GELU, the gated
+// SwiGLU / GeGLU, the backward dGELU / dSiLU (grad * act'(x)) and the gated
+// backward (two outputs: d gate, d up).
+enum : int {
+  ACT_NONE = 0, ACT_GELU = 1, ACT_SWIGLU = 2, ACT_GEGLU = 3, ACT_DGELU = 4, ACT_DSILU = 5,
+  ACT_DSWIGLU = 6, ACT_DGEGLU = 7
+};
 
 struct MxArgs {
   int M, K;                 // shape of y (the quantized matrix)
-  int tiles_m, tiles_k;     // bands of mx_band_rows() rows, 128-column steps
-  int up_col;               // SwiGLU: column of the up half in x; else 0
+  int kin;                  // input columns per output tile (K, or N of a 2N-wide output)
+  int out_half;             // output column of the second output tile (gated backward), else 0
+  int tiles_m, tiles_k;     // bands of mx_band_rows() rows, 128-column steps over kin
+  int up_col;               // column of the second operand in x2 (gated: N; else 0)
+  int up_col2;              // column of the third operand in x2 (gated backward: N)
   uint8_t* q_row;
   uint8_t* s_row;
   uint8_t* q_col;
@@ -33,12 +42,16 @@ struct MxArgs {
   uint64_t timeout_ns;
 };
 
-// TMA descriptors of one MXFP8 call: the bf16 input (box 128 columns x one
-// band) and the colwise codes [K][M] viewed as the 3-D tensor
-// [k % 8][k / 8][m] (box 128 x 16 x 8, 128-byte swizzle).
+// TMA descriptors of one MXFP8 call: the bf16 inputs (box 128 columns x one
+// band; x2 is the second input tensor, or x again) and the colwise codes
+// [K][M] viewed as the 3-D tensor [k % 8][k / 8][m] (box 128 x 16 x 8,
+// 128-byte swizzle); q_col2 covers the second output tile's rows [N, 2N) of
+// the gated backward (else q_col again).
 struct MxMaps {
   CUtensorMap x;
+  CUtensorMap x2;
   CUtensorMap q_col;
+  CUtensorMap q_col2;
 };
 
 // TMA descriptors of one NVFP4 call: the bf16 input (box 64 columns x

@@ -70,15 +70,19 @@ enum {
     MXQ_COLWISE = 2,        /* 32x1 (MX) / 16x1 (NVFP4) blocks along M,    */
                             /* stored transposed: [K][M]                   */
     MXQ_DBIAS = 4,          /* fp32 column sums of x (mx_quantize_rowcol)  */
-    MXQ_ACT_GELU_TANH = 8,  /* quantize gelu_tanh(x) (mx_quantize_rowcol)  */
-    MXQ_NVFP4_2D = 16       /* 16x16 blocks (nvfp4_quantize_transpose)     */
+    MXQ_ACT_GELU_TANH = 8,  /* gelu_tanh: of x (mx_quantize_rowcol), of the */
+                            /* gate (mx_quantize_gated: GeGLU), its         */
+                            /* derivative (mx_quantize_dact / _dgated)     */
+    MXQ_NVFP4_2D = 16,      /* 16x16 blocks (nvfp4_quantize_transpose)     */
+    MXQ_ACT_SILU = 32       /* silu: SwiGLU gate (the default of the gated */
+                            /* calls), its derivative (mx_quantize_dact)   */
 };
 
 /* bits of *dev_err */
 enum { MXQ_DEVERR_TIMEOUT = 1 };
 
 /* operation ids for mxq_workspace_bytes */
-enum { MXQ_OP_ROWCOL = 0, MXQ_OP_NVFP4 = 1 };
+enum { MXQ_OP_ROWCOL = 0, MXQ_OP_NVFP4 = 1, MXQ_OP_DACT = 2 };
 
 /* Human-readable name of a status code (static string, never NULL). */
 MXQ_API const char* mxq_status_string(int status);
@@ -151,20 +155,66 @@ MXQ_API mxq_status mx_quantize_rowcol_dbias_noalloc(const void* x, int64_t M, in
                                                     uint32_t* dev_err, mxq_stream_t stream);
 
 /*
- * mx_quantize_gated -- SwiGLU gate fused with MXFP8 quantization.
+ * mx_quantize_gated -- SwiGLU or GeGLU gate fused with MXFP8 quantization.
  *
- * Operation: y[m][n] = silu(x[m][n]) * x[m][N + n] for n < N, silu(g) =
- * g / (1 + e^-g), computed in fp32 (no intermediate bf16 rounding), then
- * quantized exactly as mx_quantize_rowcol quantizes y (TE PR #3291 table
- * "MXFP8 gated (swiglu / geglu) kernel", fusion "swiglu").
+ * Operation: y[m][n] = act(x[m][n]) * x[m][N + n] for n < N, computed in
+ * fp32 (no intermediate bf16 rounding), then quantized exactly as
+ * mx_quantize_rowcol quantizes y (TE PR #3291 table "MXFP8 gated (swiglu /
+ * geglu) kernel", fusions "swiglu" and "geglu").  act is silu(g) =
+ * g / (1 + e^-g) (SwiGLU; the default, or MXQ_ACT_SILU) or gelu_tanh
+ * (GeGLU, MXQ_ACT_GELU_TANH).
  *
  *   x       [M][ldx] bf16 holding [gate | up], each N wide; ldx >= 2N.
+ *   flags   MXQ_ROWWISE and/or MXQ_COLWISE, at most one activation flag.
  *   M % 32 == 0, N % 32 == 0.
  *   q_row [M][N], s_row [M][N/32], q_col [N][M], s_col [N][M/32] as above.
  */
 MXQ_API mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, uint32_t flags,
                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                              uint32_t* dev_err, mxq_stream_t stream);
+
+/*
+ * mx_quantize_dact -- backward activation fused with MXFP8 quantization.
+ *
+ * Operation (TE PR #3291 table "MXFP8 generic quantize kernel", fusions
+ * "dgelu", "dsilu" and "dbias_dgelu"): y[m][k] = grad[m][k] * act'(x[m][k])
+ * in fp32, with act' the derivative of gelu_tanh (MXQ_ACT_GELU_TANH) or of
+ * silu (MXQ_ACT_SILU) -- exactly one of the two; y is quantized exactly as
+ * mx_quantize_rowcol quantizes its input, and MXQ_DBIAS writes
+ * dbias[k] = sum_m y[m][k].
+ *
+ *   grad    [M][ldg] bf16, the incoming gradient; x [M][ldx] bf16, the
+ *           activation's input; M % 32 == 0, K % 32 == 0, ldg, ldx >= K,
+ *           multiples of 8, both 16-byte aligned.
+ *   outputs, dbias, workspace (mxq_workspace_bytes(MXQ_OP_DACT, M, K,
+ *           flags) bytes with MXQ_DBIAS), dev_err, stream: as for
+ *           mx_quantize_rowcol.
+ */
+MXQ_API mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t K,
+                                    int64_t ldg, int64_t ldx, uint32_t flags, uint8_t* q_row,
+                                    uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, float* dbias,
+                                    void* workspace, size_t workspace_bytes, uint32_t* dev_err,
+                                    mxq_stream_t stream);
+
+/*
+ * mx_quantize_dgated -- backward of the gated activation fused with MXFP8
+ * quantization (TE PR #3291 table "MXFP8 gated (swiglu / geglu) kernel",
+ * fusion "dswiglu", and its GeGLU counterpart).
+ *
+ * Operation: with gate = x[m][n], up = x[m][N + n] and g = grad[m][n],
+ * y[m][n] = g * up * act'(gate) (the gradient of the gate) and
+ * y[m][N + n] = g * act(gate) (the gradient of up), n < N, in fp32; act is
+ * silu (the default, or MXQ_ACT_SILU) or gelu_tanh (MXQ_ACT_GELU_TANH).  y
+ * ([M][2N]) is quantized exactly as mx_quantize_rowcol quantizes its input.
+ *
+ *   grad    [M][ldg] bf16, ldg >= N; x [M][ldx] bf16 holding [gate | up],
+ *           ldx >= 2N; M % 32 == 0, N % 32 == 0.
+ *   q_row [M][2N], s_row [M][2N/32], q_col [2N][M], s_col [2N][M/32].
+ */
+MXQ_API mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_t N,
+                                      int64_t ldg, int64_t ldx, uint32_t flags, uint8_t* q_row,
+                                      uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                      uint32_t* dev_err, mxq_stream_t stream);
 
 /*
  * bf16_amax -- largest |x| of a bf16 matrix, written as fp32 to *amax_out

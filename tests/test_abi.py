@@ -82,3 +82,30 @@ def test_gated_and_nvfp4_host_validation():
     assert L.bf16_amax(None, 16, 12, 12, None, None) == 1
     assert L.bf16_amax(None, 16, 12, 12, ctypes.c_void_p(16), None) == 2
     assert L.mxq_selftest_bounded_wait(10, None, None) == 1
+
+
+def test_backward_and_geglu_host_validation():
+    L = _lib.lib()
+    GELU, SILU = mxq.ACT_GELU_TANH, mxq.ACT_SILU
+
+    def dact(M=64, K=64, ldg=64, ldx=64, flags=3 | GELU):
+        return L.mx_quantize_dact(None, None, M, K, ldg, ldx, flags, None, None, None, None, None,
+                                  None, 0, None, None)
+
+    assert dact(flags=3) == 1                      # no activation
+    assert dact(flags=3 | GELU | SILU) == 1        # two activations
+    assert dact(flags=GELU) == 1                   # no direction
+    assert dact(flags=3 | GELU | 16) == 1          # unknown bit
+    assert dact(M=48) == 2 and dact(K=40, ldg=40, ldx=40) == 2
+    assert dact(ldg=32) == 2 and dact(ldx=32) == 2
+
+    def dgated(M=64, N=64, ldg=64, ldx=128, flags=3):
+        return L.mx_quantize_dgated(None, None, M, N, ldg, ldx, flags, None, None, None, None,
+                                    None, None)
+
+    assert dgated(flags=3 | GELU | SILU) == 1 and dgated(flags=0) == 1
+    assert dgated(ldx=100) == 2 and dgated(ldg=32) == 2 and dgated(N=48, ldg=48, ldx=96) == 2
+    assert L.mx_quantize_gated(None, 64, 64, 128, 3 | GELU | SILU, None, None, None, None, None,
+                               None) == 1
+    assert L.mxq_workspace_bytes(mxq.OP_DACT, 256, 64, mxq.DBIAS) == 2 * 64 * 4
+    assert L.mxq_workspace_bytes(mxq.OP_DACT, 256, 64, 0) == 0

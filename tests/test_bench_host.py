@@ -73,3 +73,9 @@ def test_max_over_ranks_gloo_world2():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert results == {0: 11.0, 1: 11.0}
+
+
+def test_gated_backward_byte_accounting():
+    """Gated backward: the [M, 2N] output of a plain cast plus the grad read."""
+    for M, N in ((8192, 14336), (64, 96)):
+        assert bench.dgated_bytes(M, N) == bench.mx_bytes(M, 2 * N) + 2 * M * N

@@ -132,6 +132,71 @@ def test_mx_swiglu_row_only_and_col_only():
     check_activation_blocks(host(c["q_col"]), host(c["s_col"]), ref["q_col"], ref["s_col"], 1, "col")
 
 
+def _check_mx_tol(out, ref, what):
+    for d in ("row", "col"):
+        if f"q_{d}" in ref:
+            check_activation_blocks(host(out[f"q_{d}"]), host(out[f"s_{d}"]), ref[f"q_{d}"],
+                                    ref[f"s_{d}"], 1, f"{what} {d}")
+
+
+@pytest.mark.parametrize("M,N,seed", [(256, 352, 62), (2080, 1184, 63)])
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+def test_mx_geglu(M, N, seed, flags):
+    bits = synth.swiglu(M=M, N=N, seed=seed)
+    out = mxq.mx_quantize_gated(to_device(bits), flags | mxq.ACT_GELU_TANH)
+    ref = oracle.mx_quantize_gated(bits, N, act=oracle.ACT_GELU_TANH, flags=flags)
+    _check_mx_tol(out, ref, "geglu")
+
+
+@pytest.mark.parametrize("act", ["gelu", "silu"])
+@pytest.mark.parametrize("M,K,seed,flags", [(320, 224, 64, BOTH), (2080, 1184, 65, BOTH),
+                                            (2080, 1184, 66, mxq.ROWWISE),
+                                            (2080, 1184, 67, mxq.COLWISE)])
+def test_mx_dact(act, M, K, seed, flags):
+    """grad * act'(x): both inputs N(0,1) (grad from the GELU recipe with
+    another seed)."""
+    x = synth.gelu(M=M, K=K, seed=seed)
+    grad = synth.gelu(M=M, K=K, seed=seed + 100)
+    f_gpu = mxq.ACT_GELU_TANH if act == "gelu" else mxq.ACT_SILU
+    f_orc = oracle.ACT_GELU_TANH if act == "gelu" else oracle.ACT_SILU
+    out = mxq.mx_quantize_dact(to_device(grad), to_device(x), flags | f_gpu)
+    ref = oracle.mx_quantize_dact(grad, x, f_orc, flags)
+    _check_mx_tol(out, ref, f"d{act}")
+
+
+@pytest.mark.parametrize("act", ["gelu", "silu"])
+@pytest.mark.parametrize("M,K,seed", [(320, 224, 68), (2080, 1184, 69)])
+def test_mx_dbias_dact(act, M, K, seed):
+    """dbias of y = grad * act'(x): |act'| <= 1.2 for both activations, so
+    1e-5 * 1.2 * sum|grad| bounds 1e-5 * sum|y| per column."""
+    x = synth.dbias(M=M, K=K, seed=seed)
+    grad = synth.gelu(M=M, K=K, seed=seed + 100)
+    f_gpu = mxq.ACT_GELU_TANH if act == "gelu" else mxq.ACT_SILU
+    f_orc = oracle.ACT_GELU_TANH if act == "gelu" else oracle.ACT_SILU
+    out = mxq.mx_quantize_dact(to_device(grad), to_device(x), BOTH | mxq.DBIAS | f_gpu)
+    ref = oracle.mx_quantize_dact(grad, x, f_orc, BOTH | oracle.DBIAS)
+    _check_mx_tol(out, ref, f"dbias_d{act}")
+    tol = 1.2e-5 * np.abs(synth.bf16_bits_to_f32(grad).astype(np.float64)).sum(axis=0) + 1e-30
+    err = np.abs(host(out["dbias"]).astype(np.float64) - ref["dbias"].astype(np.float64))
+    assert np.all(err <= tol), f"dbias max err {err.max()}"
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu"])
+@pytest.mark.parametrize("M,N,seed,flags", [(256, 352, 70, BOTH), (2080, 1184, 71, BOTH),
+                                            (2080, 1184, 72, mxq.ROWWISE),
+                                            (2080, 1184, 73, mxq.COLWISE)])
+def test_mx_dgated(act, M, N, seed, flags):
+    """[grad * up * act'(gate) | grad * act(gate)]; N = 352 and 1184 leave a
+    ragged last 128-column tile in each half."""
+    x = synth.swiglu(M=M, N=N, seed=seed)
+    grad = synth.gelu(M=M, K=N, seed=seed + 100)
+    f_gpu = mxq.ACT_GELU_TANH if act == "gelu" else mxq.ACT_SILU
+    f_orc = oracle.ACT_GELU_TANH if act == "gelu" else oracle.ACT_SILU
+    out = mxq.mx_quantize_dgated(to_device(grad), to_device(x), flags | f_gpu)
+    ref = oracle.mx_quantize_dgated(grad, x, N, f_orc, flags=flags)
+    _check_mx_tol(out, ref, f"d{act}glu")
+
+
 @pytest.mark.parametrize("M,K,seed", [(224, 160, 44), (32, 32, 45), (64, 64, 46), (512, 320, 47),
                                       (768, 1600, 48), (32768, 640, 61)])
 @pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
