@@ -637,25 +637,26 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         if (flush) {
           // Rowwise scale bytes of steps rsc_first..slot of this group of eight
           // (the CTA's first step for this band may fall inside the group):
-          // one 32-byte sector per row when all eight steps are present.  Warp
-          // w writes the 16 rows it quantized.
+          // one 32-byte sector per row when all eight steps are present,
+          // written by two neighbouring threads in one instruction (16 bytes
+          // each) so that the sector leaves as one request.
           const int first_tk = (pos.g == p0.g) ? p0.tk + (pos.bi < p0.bi ? 1 : 0) : 0;
           const int rsc_first = first_tk > (tk & ~7) ? (first_tk & 7) : 0;
-          const int rr = 16 * warp + lane;
-          const int row = band * BAND + rr;
-          if (lane < 16 && row < a.M) {
-            const int kb0 = (tk - slot) * 4;   // first k-block of the group
+          const int kb0 = (tk - slot) * 4;   // first k-block of the group
+          // Two 16-byte halves: every row start must be 16-byte aligned.
+          const bool full = rsc_first == 0 && slot == 7 && ((nkb | (obase >> 5)) & 15) == 0;
+          for (int it = tid; it < 2 * BAND; it += THREADS) {
+            const int rr = it >> 1, half = it & 1;
+            const int row = band * BAND + rr;
+            if (row >= a.M) continue;
             uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + (obase >> 5) + kb0;
             const uint32_t src = sbase + L::OFF_RSC + ((t * GROUP + pos.bi) * BAND + rr) * 32;
-            // Two 16-byte stores: every row start must be 16-byte aligned.
-            if (rsc_first == 0 && slot == 7 && ((nkb | (obase >> 5)) & 15) == 0) {
-              const uint4 lo = lds128(src), hi = lds128(src + 16);
-              stg128(dst, lo.x, lo.y, lo.z, lo.w);
-              stg128(dst + 16, hi.x, hi.y, hi.z, hi.w);
-            } else {
+            if (full) {
+              const uint4 v = lds128(src + 16 * half);
+              stg128(dst + 16 * half, v.x, v.y, v.z, v.w);
+            } else if (half == 0) {
               const int b_end = min((slot + 1) * 4, (a.kin >> 5) - kb0);
-              for (int bb = rsc_first * 4; bb < b_end; ++bb)
-                stg8(dst + bb, (lds32(src + (bb & ~3)) >> (8 * (bb & 3))) & 0xFFu);
+              copy_run_to_global(dst + rsc_first * 4, src + rsc_first * 4, b_end - rsc_first * 4);
             }
           }
         }

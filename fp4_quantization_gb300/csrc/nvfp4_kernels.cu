@@ -272,11 +272,6 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
     if (tid == 0 && j + NV_STAGES < count) issue_load(j + NV_STAGES);
 
-    const int col0 = tk * NV_STEP_K + 8 * c;
-    const int row0 = band * NV_BAND + 32 * warp + 8 * h;
-    const bool col_ok = col0 < a.K;
-    const bool row_ok = row0 < a.M;
-
     // 2D: the 16x16 block's amax over the four lanes that hold it, and its
     // one scale.
     uint32_t code2d = 0u;
@@ -464,26 +459,27 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
         rq_first = -1;
       }
-      // Rowwise scale bytes: eight steps = one 32-byte sector per row.
+      // Rowwise scale bytes: eight steps = one 32-byte sector per row, written
+      // by two neighbouring threads in one instruction (16 bytes each) so the
+      // sector leaves as one request.
       const int slot8 = tk & 7;
       if (rs_first < 0) rs_first = slot8;
       if (slot8 == 7 || end) {
-        const int row = band * NV_BAND + tid;
-        if (row < a.M) {
-          const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
+        const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
+        // Two 16-byte halves: every row start must be 16-byte aligned.
+        const bool full = rs_first == 0 && slot8 == 7 && (nkb & 15) == 0;
+        for (int it = tid; it < 2 * NV_BAND; it += NV_WARPS * 32) {
+          const int rr = it >> 1, half = it & 1;
+          const int row = band * NV_BAND + rr;
+          if (row >= a.M) continue;
           uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
-          const uint32_t src = sbase + NV_OFF_RSC + tid * NV_RSC_PITCH;
-          // Two 16-byte stores: every row start must be 16-byte aligned.
-          if (rs_first == 0 && slot8 == 7 && (nkb & 15) == 0) {
-            uint32_t w8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) w8[q] = lds32(src + 4 * q);
-            stg128(dst, w8[0], w8[1], w8[2], w8[3]);
-            stg128(dst + 16, w8[4], w8[5], w8[6], w8[7]);
-          } else {
+          const uint32_t src = sbase + NV_OFF_RSC + rr * NV_RSC_PITCH;
+          if (full) {
+            const uint32_t s16 = src + 16 * half;
+            stg128(dst + 16 * half, lds32(s16), lds32(s16 + 4), lds32(s16 + 8), lds32(s16 + 12));
+          } else if (half == 0) {
             const int b_end = min((slot8 + 1) * 4, nkb - kb0);
-            for (int bb = rs_first * 4; bb < b_end; ++bb)
-              stg8(dst + bb, (lds32(src + (bb & ~3)) >> (8 * (bb & 3))) & 0xFFu);
+            copy_run_to_global(dst + rs_first * 4, src + rs_first * 4, b_end - rs_first * 4);
           }
         }
         rs_first = -1;
