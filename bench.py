@@ -337,21 +337,36 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
     return out
 
 
+def cold_l2_measure(fn, steps, stream, device, flush_bytes=512 * 2 ** 20):
+    """Median per-call time with L2 flushed before every call (a 512 MiB
+    scratch buffer zeroed between calls, outside the timed events)."""
+    scratch = torch.empty(flush_bytes, dtype=torch.uint8, device=device)
+    times = []
+    for _ in range(steps):
+        scratch.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e))
+    del scratch
+    return statistics.median(times)
+
+
 def e2e_measure(mxq, bits, device, steps, warmup, stream):
-    """Same metric through the public API with host buffers: every step
-    copies the input from pinned host memory, quantizes, and copies every
-    output back to pinned host memory."""
+    """Same metric through the public API with host buffers: every step is
+    one mx_quantize_rowcol_host call, which copies the input from pinned
+    host memory to the device, quantizes it and copies every output back to
+    pinned host memory (panels pipelined inside the call)."""
     M, K = bits.shape
     x_host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    x_dev = torch.empty((M, K), dtype=torch.bfloat16, device=device)
-    outs = mxq.mx_quantize_rowcol(x_dev.copy_(x_host), mxq.ROWWISE | mxq.COLWISE)
-    host_outs = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    outs = mxq.mx_quantize_rowcol_host(x_host, mxq.ROWWISE | mxq.COLWISE)
+    ws = torch.empty(max(256, mxq.mxq_workspace_bytes(mxq.OP_ROWCOL_HOST, M, K, 3)),
+                     dtype=torch.uint8, device=device)
 
     def step():
-        x_dev.copy_(x_host, non_blocking=True)
-        mxq.mx_quantize_rowcol(x_dev, mxq.ROWWISE | mxq.COLWISE, **outs)
-        for k, v in outs.items():
-            host_outs[k].copy_(v, non_blocking=True)
+        mxq.mx_quantize_rowcol_host(x_host, mxq.ROWWISE | mxq.COLWISE, workspace=ws, **outs)
 
     for _ in range(warmup):
         step()
@@ -369,19 +384,44 @@ def e2e_measure(mxq, bits, device, steps, warmup, stream):
     return ms, h2d, d2h
 
 
-def cpu_baseline(rows=4096, K=16384):
-    """The oracle as it stands, single-threaded, on the first `rows` rows of
-    the workload (same seeded generator)."""
+def host_threads():
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_on_threads(bits, flags, threads):
+    """The oracle as it stands, on `threads` host threads: row panels (multiples
+    of 32 rows, so no block straddles two panels), one oracle call per
+    panel (the ctypes call releases the GIL).  Returns seconds."""
+    import concurrent.futures
     import oracle
+    M = bits.shape[0]
+    per = max(32, (M // threads) // 32 * 32)
+    panels = [bits[r:r + per] for r in range(0, M, per)]
+    oracle.mx_quantize(bits[:32], flags)    # load/build outside the timing
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        list(pool.map(lambda p: oracle.mx_quantize(p, flags), panels))
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(rows=4096, K=16384):
+    """The oracle as it stands on the first `rows` rows of the workload (same
+    seeded generator), on every host core (row panels, one thread each) and,
+    for reference, on one thread."""
     bits = synth.rowcol(M=rows, K=K)
-    oracle.mx_quantize(bits[:32], 3)        # load/build outside the timing
-    t0 = time.perf_counter()
-    oracle.mx_quantize(bits, 3)
-    dt = time.perf_counter() - t0
+    threads = host_threads()
+    dt = oracle_on_threads(bits, 3, threads)
+    dt1 = oracle_on_threads(bits[:rows // 4], 3, 1) * 4
     gbs = mx_bytes(rows, K) / dt / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"first {rows} of 16384 rows ({rows}x{K} bf16), rowwise+colwise, "
-                      f"{dt:.2f} s on 1 host thread"}
+                      f"{dt:.2f} s on {threads} host threads (row panels)",
+            "one_thread": {"value": round(mx_bytes(rows, K) / dt1 / 1e9, 4), "unit": "GB/s",
+                           "sample": f"first {rows // 4} rows on 1 thread, scaled x4"}}
 
 
 def gpu_arm(args):
@@ -439,12 +479,16 @@ def gpu_arm(args):
                      "kernel": "mx_quantize_kernel<rowwise|colwise>",
                      "bytes_per_launch": nbytes},
     }
+    cold_ms = cold_l2_measure(step, max(10, min(args.steps, 50)), stream, device)
+    result["cold_l2"] = {"us_per_call": round(cold_ms * 1e3, 2),
+                         "GB_per_s": round(nbytes / (cold_ms * 1e-3) / 1e9, 1),
+                         "how": "median over calls, 512 MiB zeroed before each (untimed)"}
     if args.rows:
         result["rows"] = rows_measurements(mxq, device, max(5, args.steps // 4), max(3, args.warmup),
                                            world, stream, peak)
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
-        ms, h2d, d2h = e2e_measure(mxq, bits, device, e2e_steps, 2, stream)
+        ms, h2d, d2h = e2e_measure(mxq, bits, device, e2e_steps, 3, stream)
         result["e2e"] = {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": round(ms, 4), "steps": e2e_steps}
@@ -469,19 +513,18 @@ def reference_arm(args):
     import oracle
     K = 16384
     budget_s = 90.0
-    per_row_s = 16384 * 2 / 12e6            # about 12 M elements/s per direction pair
+    threads = host_threads()
+    per_row_s = 16384 * 2 / 12e6 / threads  # about 12 M elements/s per thread and direction pair
     rows = int(budget_s / (args.steps + args.warmup) / per_row_s) // 32 * 32
     rows = max(32, min(rows, 16384))
     bits = synth.rowcol(M=rows, K=K)
     for _ in range(args.warmup):
-        oracle.mx_quantize(bits, 3)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.mx_quantize(bits, 3)
-    dt = time.perf_counter() - t0
+        oracle_on_threads(bits, 3, threads)
+    dt = sum(oracle_on_threads(bits, 3, threads) for _ in range(args.steps))
     nbytes = mx_bytes(rows, K)
     gbs = nbytes * args.steps / dt / 1e9
-    sample = f"first {rows} of 16384 rows ({rows}x{K} bf16) per step, rowwise+colwise"
+    sample = (f"first {rows} of 16384 rows ({rows}x{K} bf16) per step, rowwise+colwise, "
+              f"{threads} host threads (row panels)")
     print(json.dumps({
         "impl": "reference",
         "metric": METRIC,
@@ -498,8 +541,8 @@ def reference_arm(args):
         "data": "synthetic: N(0,1) bf16, Philox seed 5",
         "config": {"workload": "mxfp8_rowwise_colwise_16384x16384", "M": 16384, "K": K,
                    "block": 32, "directions": "rowwise+colwise"},
-        "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)

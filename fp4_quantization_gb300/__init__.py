@@ -23,6 +23,7 @@ ACT_SILU = 32
 OP_ROWCOL = 0
 OP_NVFP4 = 1
 OP_DACT = 2
+OP_ROWCOL_HOST = 3
 DEVERR_TIMEOUT = 1
 
 STATUS_NAMES = {0: "MXQ_OK", 1: "MXQ_EINVAL", 2: "MXQ_ESHAPE", 3: "MXQ_EALIGN",
@@ -126,6 +127,42 @@ def mx_quantize_rowcol_dbias_noalloc(x, flags=ROWWISE | COLWISE, *, q_row=None, 
         _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(out["dbias"]), _ptr(dev_err),
         _stream(stream))
     _check(st, "mx_quantize_rowcol_dbias_noalloc")
+    return out
+
+
+def mx_quantize_rowcol_host(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_col=None,
+                            s_col=None, workspace=None, stream=None):
+    """mx_quantize_rowcol of a bf16 matrix in host memory: outputs in host
+    memory (page-locked when allocated here), computed by panels pipelined
+    through the device.  Returns once the work is enqueued; synchronise the
+    stream before reading the outputs."""
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise TypeError("x must be a 2-D torch.bfloat16 tensor")
+    if x.is_cuda:
+        raise TypeError("x must be in host memory (use mx_quantize_rowcol for device tensors)")
+    if x.size(1) > 1 and x.stride(1) != 1:
+        raise ValueError("x needs a unit column stride")
+    M, K = x.shape
+    ldx = x.stride(0) if M > 1 else K
+
+    def host(shape, given):
+        return given if given is not None else torch.empty(shape, dtype=torch.uint8).pin_memory()
+
+    out = {}
+    if flags & ROWWISE:
+        out["q_row"] = host((M, K), q_row)
+        out["s_row"] = host((M, K // 32), s_row)
+    if flags & COLWISE:
+        out["q_col"] = host((K, M), q_col)
+        out["s_col"] = host((K, M // 32), s_col)
+    if workspace is None:
+        need = mxq_workspace_bytes(OP_ROWCOL_HOST, M, K, flags)
+        workspace = _empty((max(need, 256),), torch.uint8, torch.device("cuda"))
+    st = _lib.lib().mx_quantize_rowcol_host(
+        _ptr(x), M, K, ldx, flags, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
+        _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "mx_quantize_rowcol_host")
     return out
 
 

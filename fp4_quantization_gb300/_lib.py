@@ -24,6 +24,8 @@ SIGNATURES = {
                                           _vp, _sz, _vp, _vp]),
     "mx_quantize_rowcol_dbias_noalloc": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp,
                                                         _vp, _vp, _vp, _vp, _vp]),
+    "mx_quantize_rowcol_host": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _vp,
+                                               _vp, _sz, _vp]),
     "mx_quantize_gated": (ctypes.c_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp, _vp, _vp,
                                          _vp]),
     "mx_quantize_dact": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, _i64, _u32, _vp, _vp, _vp,

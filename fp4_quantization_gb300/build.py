@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmxq.so")
 
-SOURCES = ["mxq_api.cu", "mx_kernels.cu", "nvfp4_kernels.cu", "mxq_noalloc.cu"]
+SOURCES = ["mxq_api.cu", "mx_kernels.cu", "nvfp4_kernels.cu", "mxq_noalloc.cu", "mxq_host.cu"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -159,6 +159,7 @@ const char* mxq_status_string(int status) {
 size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags) {
   if (M <= 0 || K <= 0) return 0;
   if (op == MXQ_OP_NVFP4) return 16;   // one fp32 amax, padded
+  if (op == MXQ_OP_ROWCOL_HOST) return mxq::host_workspace_bytes(M, K);
   if ((op != MXQ_OP_ROWCOL && op != MXQ_OP_DACT) || !(flags & MXQ_DBIAS)) return 0;
   const int64_t band = mxq::mx_band_rows(op == MXQ_OP_DACT ? mxq::ACT_DGELU : mxq::ACT_NONE);
   const int64_t bands = (M + band - 1) / band;

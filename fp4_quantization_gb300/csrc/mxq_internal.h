@@ -91,6 +91,8 @@ cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two
 cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,
                              int num_sms, cudaStream_t stream);
 cudaError_t launch_nv_global_scale(const float* amax, float* global_scale, cudaStream_t stream);
+// Device workspace of mx_quantize_rowcol_host (two sets of panel buffers).
+size_t host_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, uint32_t* dev_err, cudaStream_t stream);
 
 }  // namespace mxq

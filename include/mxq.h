@@ -82,7 +82,7 @@ enum {
 enum { MXQ_DEVERR_TIMEOUT = 1 };
 
 /* operation ids for mxq_workspace_bytes */
-enum { MXQ_OP_ROWCOL = 0, MXQ_OP_NVFP4 = 1, MXQ_OP_DACT = 2 };
+enum { MXQ_OP_ROWCOL = 0, MXQ_OP_NVFP4 = 1, MXQ_OP_DACT = 2, MXQ_OP_ROWCOL_HOST = 3 };
 
 /* Human-readable name of a status code (static string, never NULL). */
 MXQ_API const char* mxq_status_string(int status);
@@ -153,6 +153,35 @@ MXQ_API mxq_status mx_quantize_rowcol_dbias_noalloc(const void* x, int64_t M, in
                                                     uint8_t* s_row, uint8_t* q_col,
                                                     uint8_t* s_col, float* dbias,
                                                     uint32_t* dev_err, mxq_stream_t stream);
+
+/*
+ * mx_quantize_rowcol_host -- mx_quantize_rowcol on a matrix in host memory.
+ * The pages have no counterpart: it is the path for callers whose data is
+ * on the host, and what the benchmark's end-to-end figure measures.
+ *
+ * The same cast (plain, no dbias or activation) of x in row panels of up to
+ * 2048 rows: each panel is copied to the device, quantized, and its outputs
+ * copied back (colwise codes and scales as 2-D copies into the [K][M] and
+ * [K][M/32] host layouts); two sets of device buffers alternate and the
+ * copies run on two library-owned streams, so copies in, casts and copies
+ * out of consecutive panels overlap.
+ *
+ *   x, q_row, s_row, q_col, s_col  host memory with the layouts of
+ *           mx_quantize_rowcol; page-locked memory lets the copies run
+ *           asynchronously (pageable memory works, without overlap).
+ *   flags   MXQ_ROWWISE and/or MXQ_COLWISE.
+ *   workspace  device memory, 256-byte aligned, at least
+ *           mxq_workspace_bytes(MXQ_OP_ROWCOL_HOST, M, K, flags) bytes.
+ *   stream  the call starts after the work already on `stream`, and work
+ *           enqueued on `stream` afterwards starts after the outputs are on
+ *           the host (synchronise the stream before reading them).
+ * Calls from several host threads are serialised inside the library (they
+ * share the per-device streams).
+ */
+MXQ_API mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                           uint32_t flags, uint8_t* q_row, uint8_t* s_row,
+                                           uint8_t* q_col, uint8_t* s_col, void* workspace,
+                                           size_t workspace_bytes, mxq_stream_t stream);
 
 /*
  * mx_quantize_gated -- SwiGLU or GeGLU gate fused with MXFP8 quantization.

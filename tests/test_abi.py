@@ -109,3 +109,22 @@ def test_backward_and_geglu_host_validation():
                                None) == 1
     assert L.mxq_workspace_bytes(mxq.OP_DACT, 256, 64, mxq.DBIAS) == 2 * 64 * 4
     assert L.mxq_workspace_bytes(mxq.OP_DACT, 256, 64, 0) == 0
+
+
+def test_host_path_host_validation():
+    L = _lib.lib()
+
+    def call(M=64, K=64, ldx=64, flags=3, ws=None, ws_bytes=0):
+        return L.mx_quantize_rowcol_host(ctypes.c_void_p(16), M, K, ldx, flags,
+                                         ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                         ctypes.c_void_p(16), ctypes.c_void_p(16), ws, ws_bytes,
+                                         None)
+
+    assert call(flags=0) == 1 and call(flags=3 | mxq.DBIAS) == 1
+    assert call(M=48) == 2 and call(ldx=32) == 2
+    assert call() == 5                                     # no workspace
+    need = L.mxq_workspace_bytes(mxq.OP_ROWCOL_HOST, 64, 64, 3)
+    assert need > 0
+    assert call(ws=ctypes.c_void_p(256), ws_bytes=need - 1) == 5
+    assert call(ws=ctypes.c_void_p(128), ws_bytes=need) == 3   # not 256-byte aligned
+    assert call(M=0) == 0

@@ -65,6 +65,33 @@ def test_mx_rowcol_cta_ranges(M, K, seed, flags):
         assert_equal_bytes(host(out[key]), ref[key], f"{M}x{K} {key}")
 
 
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_mx_rowcol_host_buffers(flags, pinned):
+    """The host-buffer entry point: three row panels (2048, 2048, 96 rows),
+    ragged K, outputs equal to the device path's byte for byte."""
+    bits = synth.rowcol(M=4192, K=1056, seed=74)
+    x_host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    if pinned:
+        x_host = x_host.pin_memory()
+    out = mxq.mx_quantize_rowcol_host(x_host, flags)
+    torch.cuda.synchronize()
+    ref = mxq.mx_quantize_rowcol(to_device(bits), flags)
+    for key in ref:
+        assert_equal_bytes(out[key].numpy(), host(ref[key]), f"host path {key}")
+
+
+def test_mx_rowcol_host_strided_window():
+    """ldx > K: a column window of a wider host matrix, one panel."""
+    full = synth.rowcol(M=256, K=640, seed=75)
+    x_host = torch.from_numpy(full.view(np.int16)).view(torch.bfloat16)[:, 64:64 + 512]
+    out = mxq.mx_quantize_rowcol_host(x_host, BOTH)
+    torch.cuda.synchronize()
+    ref = oracle.mx_quantize(full[:, 64:64 + 512], BOTH)
+    for key in ref:
+        assert_equal_bytes(out[key].numpy(), ref[key], f"host window {key}")
+
+
 def test_mx_rowcol_strided_input():
     """ldx > K: a column window of a wider matrix."""
     full = synth.rowcol(M=128, K=512, seed=35)
