@@ -26,6 +26,10 @@ Workload recipes (distribution, structure and default sizes):
                     up N(0,1), seed 3.
 * ``gelu``          8192x14336 N(0,1), seed 3 (its own stream).
 * ``nvfp4``         16384x8192 N(0,1), 0.1% of entries times 100, seed 4.
+* ``device_normal`` any M x K N(0,1) drawn on a CUDA device with torch's
+                    seeded generator (for sizes past 2^31 elements, where a
+                    host draw would cost minutes); returned as a bf16 device
+                    tensor whose windows are copied back for checking.
 """
 import numpy as np
 
@@ -138,3 +142,18 @@ WORKLOADS = {
     "gelu": gelu,
     "nvfp4": nvfp4,
 }
+
+
+def device_normal(M, K, seed, device="cuda", chunk_rows=4096):
+    """M x K N(0,1) bf16 drawn on `device` (torch's Philox, seeded), rounded
+    once from float32 to bf16 (round to nearest even), chunk_rows rows at a
+    time."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, M, chunk_rows):
+        r1 = min(M, r0 + chunk_rows)
+        out[r0:r1] = torch.randn((r1 - r0, K), generator=g, device=device,
+                                 dtype=torch.float32).to(torch.bfloat16)
+    return out

@@ -151,3 +151,55 @@ def test_nvfp4_2d_16384x8192():
                            f"2d q_t ({m0},{k0})")
         assert_equal_bytes(host(out["s_t"][k0:k0 + 128, m0 // 16:(m0 + 64) // 16]), ref["s_t"],
                            f"2d s_t ({m0},{k0})")
+
+
+def _device_window(x, m0, k0, h, w):
+    return x[m0:m0 + h, k0:k0 + w].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _edge_windows(M, K, h, w, n, seed, align):
+    """Random windows plus the four corners (the last rows and columns are
+    where a 32-bit index would have wrapped)."""
+    return windows(M, K, h, w, n, seed, align) + [(0, 0), (0, K - w), (M - h, 0), (M - h, K - w)]
+
+
+def test_rowcol_past_2e31_elements():
+    """65536 x 32768 = 2^31 elements (4 GiB of bf16): element and byte
+    offsets above 2^31 in every output."""
+    M, K = 65536, 32768
+    x = synth.device_normal(M, K, seed=76)
+    out = mxq.mx_quantize_rowcol(x, BOTH)
+    torch.cuda.synchronize()
+    for m0, k0 in _edge_windows(M, K, 32, 256, 12, seed=8, align=32):
+        bits = _device_window(x, m0, k0, 32, 256)
+        ref = oracle.mx_quantize(bits, BOTH)
+        assert_equal_bytes(host(out["q_row"][m0:m0 + 32, k0:k0 + 256]), ref["q_row"], f"q_row ({m0},{k0})")
+        assert_equal_bytes(host(out["s_row"][m0:m0 + 32, k0 // 32:(k0 + 256) // 32]), ref["s_row"],
+                           f"s_row ({m0},{k0})")
+        assert_equal_bytes(host(out["q_col"][k0:k0 + 256, m0:m0 + 32]), ref["q_col"], f"q_col ({m0},{k0})")
+        assert_equal_bytes(host(out["s_col"][k0:k0 + 256, m0 // 32:(m0 + 32) // 32]), ref["s_col"],
+                           f"s_col ({m0},{k0})")
+    del x, out
+    torch.cuda.empty_cache()
+
+
+def test_nvfp4_past_2e31_elements():
+    """65536 x 32768 NVFP4 (1D), tensor amax computed on the device."""
+    M, K = 65536, 32768
+    x = synth.device_normal(M, K, seed=77)
+    out = mxq.nvfp4_quantize_transpose(x, BOTH)
+    A = float(host(mxq.bf16_amax(x))[0])
+    assert A == float(x.abs().max().float().item())
+    for m0, k0 in _edge_windows(M, K, 64, 128, 12, seed=9, align=16):
+        bits = _device_window(x, m0, k0, 64, 128)
+        ref = oracle.nvfp4_quantize(bits, tensor_amax=A)
+        assert_equal_bytes(host(out["q_row"][m0:m0 + 64, k0 // 2:(k0 + 128) // 2]), ref["q_row"],
+                           f"q_row ({m0},{k0})")
+        assert_equal_bytes(host(out["s_row"][m0:m0 + 64, k0 // 16:(k0 + 128) // 16]), ref["s_row"],
+                           f"s_row ({m0},{k0})")
+        assert_equal_bytes(host(out["q_t"][k0:k0 + 128, m0 // 2:(m0 + 64) // 2]), ref["q_t"],
+                           f"q_t ({m0},{k0})")
+        assert_equal_bytes(host(out["s_t"][k0:k0 + 128, m0 // 16:(m0 + 64) // 16]), ref["s_t"],
+                           f"s_t ({m0},{k0})")
+    del x, out
+    torch.cuda.empty_cache()
