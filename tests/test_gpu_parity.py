@@ -317,6 +317,32 @@ def test_nvfp4_2d_caller_amax_and_wide_range(amax_factor):
         assert_equal_bytes(host(out[key]), ref[key], f"2d amax x{amax_factor} {key}")
 
 
+def test_sharded_helpers_single_rank_nccl():
+    """The sharded helpers through NCCL on a one-rank group (this box has one
+    GPU): the collectives pass device tensors and the results equal the
+    unsharded calls."""
+    import socket
+    import torch.distributed as dist
+    from fp4_quantization_gb300 import sharded
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        bits = synth.nvfp4(M=256, K=512, seed=78)
+        x = to_device(bits)
+        got = sharded.nvfp4_quantize_transpose_sharded(x, BOTH)
+        want = mxq.nvfp4_quantize_transpose(x, BOTH)
+        for key in ("q_row", "s_row", "q_t", "s_t", "global_scale"):
+            assert torch.equal(got[key], want[key]), key
+        got = sharded.mx_quantize_rowcol_dbias_sharded(x, BOTH)
+        want = mxq.mx_quantize_rowcol(x, BOTH | mxq.DBIAS)
+        for key in want:
+            assert torch.equal(got[key], want[key]), key
+    finally:
+        dist.destroy_process_group()
+
+
 @pytest.mark.parametrize("M,K", [(96, 256), (1, 8), (333, 72)])
 def test_bf16_amax(M, K):
     bits = synth.nvfp4(M=max(M, 16), K=max(K, 16), seed=48)[:M, :K].copy()
