@@ -225,8 +225,8 @@ struct MxLayout {
 // ---------------------------------------------------------------------------
 
 template <int MODE, bool DBIAS, int ACT, int WARPS, int STAGES, int GROUP, int QBUF,
-          int CPITCH>
-__global__ void __launch_bounds__(WARPS * 32, 1)
+          int CPITCH, int CPS>
+__global__ void __launch_bounds__(WARPS * 32, CPS)
 mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_x2,
                    const __grid_constant__ CUtensorMap tmap_qcol,
@@ -713,8 +713,11 @@ dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __r
 // Launch configuration per variant
 // ---------------------------------------------------------------------------
 
-// Warps per CTA (= 16-row slices of a band) and ring slots; one CTA per
-// SM.  Overridable at build time for tuning sweeps.
+// Warps per CTA (= 16-row slices of a band), ring slots and resident CTAs
+// per SM, overridable at build time for tuning sweeps.  Measured on GB300:
+// the plain cast runs best with one CTA per SM and three slots (two CTAs of
+// two slots each: 214 vs 196 us); GELU with two CTAs per SM of two slots
+// each (108 vs 112 us: one CTA's barriers no longer stall the whole SM).
 #ifndef MXQ_PLAIN_WARPS
 #define MXQ_PLAIN_WARPS 8
 #endif
@@ -725,7 +728,7 @@ dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __r
 #define MXQ_GELU_WARPS 8
 #endif
 #ifndef MXQ_GELU_STAGES
-#define MXQ_GELU_STAGES 4
+#define MXQ_GELU_STAGES 2
 #endif
 #ifndef MXQ_SWIGLU_WARPS
 #define MXQ_SWIGLU_WARPS 8
@@ -742,6 +745,9 @@ dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __r
 #ifndef MXQ_PLAIN_QBUF
 #define MXQ_PLAIN_QBUF 1
 #endif
+#ifndef MXQ_PLAIN_CPS
+#define MXQ_PLAIN_CPS 1
+#endif
 #ifndef MXQ_GELU_GROUP
 #define MXQ_GELU_GROUP 1
 #endif
@@ -750,6 +756,9 @@ dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __r
 #endif
 #ifndef MXQ_GELU_QBUF
 #define MXQ_GELU_QBUF 1
+#endif
+#ifndef MXQ_GELU_CPS
+#define MXQ_GELU_CPS 2
 #endif
 #ifndef MXQ_SWIGLU_GROUP
 #define MXQ_SWIGLU_GROUP 1
@@ -760,6 +769,9 @@ dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __r
 #ifndef MXQ_SWIGLU_QBUF
 #define MXQ_SWIGLU_QBUF 1
 #endif
+#ifndef MXQ_SWIGLU_CPS
+#define MXQ_SWIGLU_CPS 1
+#endif
 template <int ACT>
 struct MxConfig {   // plain / dbias: band of 16 * WARPS rows
   static constexpr int WARPS = MXQ_PLAIN_WARPS;
@@ -767,6 +779,7 @@ struct MxConfig {   // plain / dbias: band of 16 * WARPS rows
   static constexpr int GROUP = MXQ_PLAIN_GROUP;          // with rowwise output
   static constexpr int GROUP_COL = MXQ_PLAIN_GROUP_COL;  // colwise only
   static constexpr int QBUF = MXQ_PLAIN_QBUF;            // colwise staging buffers
+  static constexpr int CPS = MXQ_PLAIN_CPS;              // resident CTAs per SM
 };
 template <>
 struct MxConfig<ACT_GELU> {
@@ -775,6 +788,7 @@ struct MxConfig<ACT_GELU> {
   static constexpr int GROUP = MXQ_GELU_GROUP;          // with rowwise output
   static constexpr int GROUP_COL = MXQ_GELU_GROUP_COL;  // colwise only
   static constexpr int QBUF = MXQ_GELU_QBUF;            // colwise staging buffers
+  static constexpr int CPS = MXQ_GELU_CPS;              // resident CTAs per SM
 };
 template <>
 struct MxConfig<ACT_SWIGLU> {   // gate + up per slot
@@ -783,6 +797,7 @@ struct MxConfig<ACT_SWIGLU> {   // gate + up per slot
   static constexpr int GROUP = MXQ_SWIGLU_GROUP;          // with rowwise output
   static constexpr int GROUP_COL = MXQ_SWIGLU_GROUP_COL;  // colwise only
   static constexpr int QBUF = MXQ_SWIGLU_QBUF;            // colwise staging buffers
+  static constexpr int CPS = MXQ_SWIGLU_CPS;              // resident CTAs per SM
 };
 // The other two-operand paths (GeGLU; grad + x of the backward fusions)
 // share the SwiGLU configuration.
@@ -800,6 +815,7 @@ struct MxConfigDGated {
   static constexpr int GROUP = 1;
   static constexpr int GROUP_COL = 1;
   static constexpr int QBUF = 1;
+  static constexpr int CPS = 1;
 };
 template <>
 struct MxConfig<ACT_DSWIGLU> : MxConfigDGated {};
@@ -815,13 +831,16 @@ cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
   // colwise-only cast gains from interleaving bands (longer colwise runs).
   constexpr int GROUP = (MODE & MX_ROW) ? MxConfig<ACT>::GROUP : MxConfig<ACT>::GROUP_COL;
   constexpr int QBUF = MxConfig<ACT>::QBUF;
+  // Band groups (colwise-only) need more staging than two CTAs can share.
+  constexpr int CPS = GROUP == 1 ? MxConfig<ACT>::CPS : 1;
   // Column pitch of the colwise scale staging (four blocks per column).  The
   // pitch changes how the warps' store phases line up; measured on GB300,
   // 8 bytes is faster for the plain cast and 4 bytes for the fused paths.
   constexpr int CPITCH = (ACT == ACT_NONE && !DBIAS) ? 8 : 4;
   using L = MxLayout<WARPS, act_operands(ACT), STAGES, GROUP, QBUF, CPITCH, act_outputs(ACT)>;
   static_assert(L::DYNAMIC <= 227 * 1024, "shared memory per CTA");
-  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS, STAGES, GROUP, QBUF, CPITCH>;
+  static_assert(CPS == 1 || CPS * (L::DYNAMIC + 1024) <= 228 * 1024, "CTAs per SM must fit");
+  auto kernel = mx_quantize_kernel<MODE, DBIAS, ACT, WARPS, STAGES, GROUP, QBUF, CPITCH, CPS>;
 
   static int configured_device = -1;
   int dev = 0;
@@ -833,7 +852,8 @@ cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
     configured_device = dev;
   }
   const int64_t steps = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
-  const int grid = static_cast<int>(steps < num_sms ? steps : num_sms);
+  const int64_t slots = static_cast<int64_t>(CPS) * num_sms;   // persistent CTAs
+  const int grid = static_cast<int>(steps < slots ? steps : slots);
   kernel<<<grid < 1 ? 1 : grid, WARPS * 32, L::DYNAMIC, stream>>>(maps.x, maps.x2, maps.q_col,
                                                                    maps.q_col2, a);
   return cudaGetLastError();
