@@ -96,6 +96,17 @@ mxq_status encode_mx_qcol_map(CUtensorMap* map, int64_t M, int64_t K, uint8_t* q
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Rowwise-code map: `width` columns of a [M][pitch] byte matrix starting at
+// base, box 128 columns x `band` rows, 128-byte swizzle.
+mxq_status encode_mx_qrow_map(CUtensorMap* map, uint8_t* base, int64_t M, int64_t width,
+                              int64_t pitch, int band) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(mxq::MX_TILE_K), static_cast<cuuint32_t>(band)};
+  return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // NVFP4 code maps: rowwise [M][K/2] seen as [m % 8][m / 8][k / 2] (box
 // 128 B x band / 8 x 8) and transposed [K][M/2] seen as [k % 8][k / 8][m / 2]
 // (box 128 B x step / 8 x 8), both with the 128-byte swizzle.
@@ -223,6 +234,11 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
     if (st != MXQ_OK) return st;
   }
   maps.q_col2 = maps.q_col;
+  if (flags & MXQ_ROWWISE) {
+    st = encode_mx_qrow_map(&maps.q_row, q_row, M, K, K, band);
+    if (st != MXQ_OK) return st;
+  }
+  maps.q_row2 = maps.q_row;
   st = from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
   if (st != MXQ_OK || !want_dbias) return st;
   return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
@@ -274,6 +290,11 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
     if (st != MXQ_OK) return st;
   }
   maps.q_col2 = maps.q_col;
+  if (flags & MXQ_ROWWISE) {
+    st = encode_mx_qrow_map(&maps.q_row, q_row, M, N, N, band);
+    if (st != MXQ_OK) return st;
+  }
+  maps.q_row2 = maps.q_row;
   return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, act, sms, stream));
 }
 
@@ -336,6 +357,11 @@ mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t 
     if (st != MXQ_OK) return st;
   }
   maps.q_col2 = maps.q_col;
+  if (flags & MXQ_ROWWISE) {
+    st = encode_mx_qrow_map(&maps.q_row, q_row, M, K, K, band);
+    if (st != MXQ_OK) return st;
+  }
+  maps.q_row2 = maps.q_row;
   st = from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
   if (st != MXQ_OK || !want_dbias) return st;
   return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
@@ -390,6 +416,13 @@ mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_
     st = encode_mx_qcol_map(&maps.q_col, M, N, q_col);
     if (st != MXQ_OK) return st;
     st = encode_mx_qcol_map(&maps.q_col2, M, N, q_col + static_cast<size_t>(N) * M);
+    if (st != MXQ_OK) return st;
+  }
+  if (flags & MXQ_ROWWISE) {
+    // Likewise for the rowwise codes: columns [0, N) and [N, 2N) of [M][2N].
+    st = encode_mx_qrow_map(&maps.q_row, q_row, M, N, 2 * N, band);
+    if (st != MXQ_OK) return st;
+    st = encode_mx_qrow_map(&maps.q_row2, q_row + N, M, N, 2 * N, band);
     if (st != MXQ_OK) return st;
   }
   return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, act, sms, stream));

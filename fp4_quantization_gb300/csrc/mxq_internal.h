@@ -52,6 +52,11 @@ struct MxMaps {
   CUtensorMap x2;
   CUtensorMap q_col;
   CUtensorMap q_col2;
+  // Rowwise codes [M][K] (box 128 columns x one band, 128-byte swizzle);
+  // q_row2 covers the second output tile's columns [N, 2N) of the gated
+  // backward, and q_row its first N columns (else q_row again).
+  CUtensorMap q_row;
+  CUtensorMap q_row2;
 };
 
 // TMA descriptors of one NVFP4 call: the bf16 input (box 64 columns x
