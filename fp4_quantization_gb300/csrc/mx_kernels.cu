@@ -763,6 +763,12 @@ dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __r
 #ifndef MXQ_PLAIN_GROUP
 #define MXQ_PLAIN_GROUP 1
 #endif
+#ifndef MXQ_DBIAS_STAGES
+#define MXQ_DBIAS_STAGES 4   // dbias 8192^2: 60.5 us (3 slots: 63 us; 2 CTAs/SM x 2: 64.6 us)
+#endif
+#ifndef MXQ_DBIAS_CPS
+#define MXQ_DBIAS_CPS 1
+#endif
 #ifndef MXQ_PLAIN_GROUP_COL
 #define MXQ_PLAIN_GROUP_COL 8
 #endif
@@ -850,13 +856,14 @@ template <int MODE, bool DBIAS, int ACT>
 cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
                            cudaStream_t stream) {
   constexpr int WARPS = MxConfig<ACT>::WARPS;
-  constexpr int STAGES = MxConfig<ACT>::STAGES;
+  constexpr bool PLAIN_DBIAS = DBIAS && ACT == ACT_NONE;   // its own ring / residency
+  constexpr int STAGES = PLAIN_DBIAS ? MXQ_DBIAS_STAGES : MxConfig<ACT>::STAGES;
   // Rowwise code lines want each CTA to stay on one band along K; the
   // colwise-only cast gains from interleaving bands (longer colwise runs).
   constexpr int GROUP = (MODE & MX_ROW) ? MxConfig<ACT>::GROUP : MxConfig<ACT>::GROUP_COL;
   constexpr int QBUF = MxConfig<ACT>::QBUF;
   // Band groups (colwise-only) need more staging than two CTAs can share.
-  constexpr int CPS = GROUP == 1 ? MxConfig<ACT>::CPS : 1;
+  constexpr int CPS = GROUP != 1 ? 1 : PLAIN_DBIAS ? MXQ_DBIAS_CPS : MxConfig<ACT>::CPS;
   // Column pitch of the colwise scale staging (four blocks per column).  The
   // pitch changes how the warps' store phases line up; measured on GB300,
   // 8 bytes is faster for the plain cast and 4 bytes for the fused paths.
