@@ -17,6 +17,7 @@ from . import build as _build
 
 ROWWISE, COLWISE, DBIAS = 1, 2, 4
 NVFP4_2D = 16
+SCALE_RCEIL = 64
 ACT_NONE, ACT_GELU_TANH, ACT_SILU = 0, 1, 2
 
 _lib = None
@@ -44,7 +45,8 @@ def lib():
         L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
         L.orc_e8m0_code.restype = ctypes.c_uint8
         L.orc_e8m0_code.argtypes = [ctypes.c_double]
-        for name in ("orc_e4m3_encode_array", "orc_e2m1_encode_array", "orc_e8m0_code_array"):
+        for name in ("orc_e4m3_encode_array", "orc_e2m1_encode_array", "orc_e8m0_code_array",
+                     "orc_e8m0_code_rceil_array"):
             fn = getattr(L, name)
             fn.restype = None
             fn.argtypes = [dp, i64, u8p]
@@ -123,6 +125,14 @@ def e8m0_code(amax):
     v = np.ascontiguousarray(amax, dtype=np.float64).ravel()
     out = np.empty(v.size, np.uint8)
     lib().orc_e8m0_code_array(v.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), v.size, _u8(out))
+    return out
+
+
+def e8m0_code_rceil(amax):
+    v = np.ascontiguousarray(amax, dtype=np.float64).ravel()
+    out = np.empty(v.size, np.uint8)
+    lib().orc_e8m0_code_rceil_array(v.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), v.size,
+                                    _u8(out))
     return out
 
 

@@ -25,6 +25,10 @@
  *    The multiply by 2^-e is the "inverse scale" of torchao PR #12 (its
  *    rationale section): one reciprocal per block, then a multiply per
  *    element; here the reciprocal is an exact power of two.
+ *    With ORC_SCALE_RCEIL the shared exponent follows the ceil-style rule
+ *    instead: e = ceil(log2(a / 448)), the smallest power of two for which
+ *    no element of the block exceeds 448 (so nothing saturates), clamped
+ *    the same way.
  *
  *  Activations (TE PR #3291, "MXFP8 generic" fusion "gelu" and "MXFP8 gated"
  *  fusion "swiglu"): y is computed in double and rounded once to fp32, then
@@ -188,6 +192,23 @@ void orc_e2m1_encode_array(const double* v, int64_t n, uint8_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_encode(v[i]);
 }
 
+/* The ceil-style rule: e = ceil(log2(amax / 448)), the smallest power of two
+ * for which no element of the block exceeds the E4M3 maximum 448, clamped
+ * to [-127, 127]; amax = 0 gives code 0. */
+uint8_t orc_e8m0_code_rceil(double amax) {
+    if (isnan(amax)) return 0xFF;
+    if (!(amax > 0.0)) return 0;
+    if (isinf(amax)) return 0xFE;
+    double e = ceil(log2(amax / 448.0));
+    if (e < -127.0) e = -127.0;
+    if (e > 127.0) e = 127.0;
+    return (uint8_t)((int)e + 127);
+}
+
+void orc_e8m0_code_rceil_array(const double* amax, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e8m0_code_rceil(amax[i]);
+}
+
 void orc_e8m0_code_array(const double* amax, int64_t n, uint8_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_e8m0_code(amax[i]);
 }
@@ -272,13 +293,14 @@ float orc_dsilu(float x) {
 
 /* Quantize one MX block of 32 fp32 values.  y[i * ys] are the values,
  * q[i * qs] receive the E4M3 codes, *scale the E8M0 code. */
-static void mx_block(const float* y, int64_t ys, uint8_t* q, int64_t qs, uint8_t* scale) {
+static void mx_block(const float* y, int64_t ys, uint8_t* q, int64_t qs, uint8_t* scale,
+                     int rceil) {
     double amax = 0.0;
     for (int i = 0; i < 32; ++i) {
         double a = fabs((double)y[i * ys]);
         if (a > amax) amax = a;
     }
-    uint8_t code = orc_e8m0_code(amax);
+    uint8_t code = rceil ? orc_e8m0_code_rceil(amax) : orc_e8m0_code(amax);
     int e = (int)code - 127;
     *scale = code;
     for (int i = 0; i < 32; ++i) {
@@ -295,13 +317,13 @@ static void mx_quantize_dense(const float* y, int64_t M, int64_t K, int flags,
         for (int64_t m = 0; m < M; ++m)
             for (int64_t kb = 0; kb < K / 32; ++kb)
                 mx_block(y + m * K + kb * 32, 1, q_row + m * K + kb * 32, 1,
-                         s_row + m * (K / 32) + kb);
+                         s_row + m * (K / 32) + kb, flags & ORC_SCALE_RCEIL);
     }
     if (flags & ORC_COLWISE) {
         for (int64_t k = 0; k < K; ++k)
             for (int64_t mb = 0; mb < M / 32; ++mb)
                 mx_block(y + mb * 32 * K + k, K, q_col + k * M + mb * 32, 1,
-                         s_col + k * (M / 32) + mb);
+                         s_col + k * (M / 32) + mb, flags & ORC_SCALE_RCEIL);
     }
 }
 

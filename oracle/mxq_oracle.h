@@ -33,7 +33,7 @@
 extern "C" {
 #endif
 
-enum { ORC_ROWWISE = 1, ORC_COLWISE = 2, ORC_DBIAS = 4, ORC_NVFP4_2D = 16 };
+enum { ORC_ROWWISE = 1, ORC_COLWISE = 2, ORC_DBIAS = 4, ORC_NVFP4_2D = 16, ORC_SCALE_RCEIL = 64 };
 enum { ORC_ACT_NONE = 0, ORC_ACT_GELU_TANH = 1, ORC_ACT_SILU = 2 };
 
 /* Scalar format conversions. */
@@ -43,11 +43,13 @@ double  orc_e4m3_decode(uint8_t code);
 uint8_t orc_e2m1_encode(double v);      /* RNE, saturate to +-6, keep sign */
 double  orc_e2m1_decode(uint8_t code);
 uint8_t orc_e8m0_code(double amax);     /* MX shared-scale rule, see .c */
+uint8_t orc_e8m0_code_rceil(double amax);   /* ceil rule (flag ORC_SCALE_RCEIL) */
 
 /* Array forms of the encoders, for brute-force tests. */
 void orc_e4m3_encode_array(const double* v, int64_t n, uint8_t* out);
 void orc_e2m1_encode_array(const double* v, int64_t n, uint8_t* out);
 void orc_e8m0_code_array(const double* amax, int64_t n, uint8_t* out);
+void orc_e8m0_code_rceil_array(const double* amax, int64_t n, uint8_t* out);
 
 /* Activations and derivatives evaluated in double and rounded once to fp32. */
 float orc_gelu_tanh(float x);

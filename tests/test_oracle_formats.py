@@ -192,3 +192,21 @@ def test_bf16_decode_all_patterns():
             assert math.isnan(got)
         else:
             assert got == want[b], hex(b)
+
+
+def test_e8m0_rceil_is_the_smallest_non_saturating_scale():
+    """Ceil rule over every positive finite bf16 amax: 2^e is the smallest
+    power of two with amax / 2^e <= 448 (clamped at e = -127), and it equals
+    the integer form max(0, E - 8 + [mantissa > 1.75]) on the bf16 fields."""
+    bits = np.arange(1, 0x7F80, dtype=np.uint32)               # positive, finite
+    amax = (bits << 16).view(np.float32).astype(np.float64)
+    codes = oracle.e8m0_code_rceil(amax).astype(np.int64)
+    e = codes - 127
+    assert np.all(amax / np.exp2(e.astype(np.float64)) <= 448.0)
+    above = e > -127
+    assert np.all(amax[above] / np.exp2(e[above] - 1.0) > 448.0)
+    E = (bits >> 7).astype(np.int64)
+    mant = (bits & 0x7F).astype(np.int64)
+    assert np.array_equal(codes, np.maximum(0, E - 8 + (mant > 0x60)))
+    assert oracle.e8m0_code_rceil([0.0])[0] == 0
+    assert oracle.e8m0_code_rceil([448.0])[0] == 127 and oracle.e8m0_code_rceil([449.0])[0] == 128

@@ -475,3 +475,27 @@ def test_nvfp4_2d_reduces_to_1d_on_repeated_rows_and_columns():
     one = oracle.nvfp4_quantize(cols, tensor_amax=A, flags=3)
     np.testing.assert_array_equal(two["q_t"], one["q_t"])
     np.testing.assert_array_equal(two["s_t"], one["s_t"])
+
+
+def test_mx_rceil_blocks_never_saturate():
+    """With the ceil rule every block's largest element maps to at most 448
+    (no saturation), the scale is the pinned ceil code of the block amax, and
+    the codes are the pinned E4M3 encoder's."""
+    x = synth.dbias(M=64, K=96, seed=23)
+    out = oracle.mx_quantize(x, oracle.ROWWISE | oracle.COLWISE | oracle.SCALE_RCEIL)
+    y = f32(x)
+    for m in range(64):
+        for kb in range(3):
+            blk = y[m, kb * 32:(kb + 1) * 32]
+            code = oracle.e8m0_code_rceil([np.abs(blk).max()])[0]
+            assert out["s_row"][m, kb] == code
+            v = np.ldexp(blk, 127 - int(code))
+            assert np.abs(v).max() <= 448.0
+            np.testing.assert_array_equal(out["q_row"][m, kb * 32:(kb + 1) * 32], oracle.e4m3_encode(v))
+    for k in range(96):
+        for mb in range(2):
+            blk = y[mb * 32:(mb + 1) * 32, k]
+            code = oracle.e8m0_code_rceil([np.abs(blk).max()])[0]
+            assert out["s_col"][k, mb] == code
+            np.testing.assert_array_equal(out["q_col"][k, mb * 32:(mb + 1) * 32],
+                                          oracle.e4m3_encode(np.ldexp(blk, 127 - int(code))))
