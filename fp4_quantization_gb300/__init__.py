@@ -20,6 +20,7 @@ DBIAS = 4
 ACT_GELU_TANH = 8
 NVFP4_2D = 16
 ACT_SILU = 32
+SCALE_RCEIL = 64
 OP_ROWCOL = 0
 OP_NVFP4 = 1
 OP_DACT = 2

@@ -183,6 +183,22 @@ __device__ __forceinline__ uint32_t half16(uint32_t pair, int which) {
 // Exponent fields of a packed pair of bf16 magnitudes, as two 16-bit lanes.
 __device__ __forceinline__ uint32_t bf16_exponents(uint32_t m) { return (m >> 7) & 0x00FF00FFu; }
 
+// Scale exponents of a packed pair of bf16 magnitudes under the selected
+// rule: the exponent field (floor rule), plus one where the significand is
+// above 1.75 when ceil_mask is all ones (ceil rule: 2^(E-127) * m > 448 *
+// 2^(E-135) exactly when m > 1.75, so E - 8 + [m > 1.75] is
+// ceil(log2(amax / 448)) + 127).  The code is monotone in the amax, so
+// block maxima may be combined on these values.
+__device__ __forceinline__ uint32_t bf16_scale_exponents(uint32_t m, uint32_t ceil_mask) {
+  const uint32_t bump = (((m & 0x7Fu) > 0x60u) ? 1u : 0u) | ((((m >> 16) & 0x7Fu) > 0x60u) ? 0x10000u : 0u);
+  return bf16_exponents(m) + (bump & ceil_mask);
+}
+
+// The same for one fp32 magnitude (bits without the sign).
+__device__ __forceinline__ uint32_t f32_scale_exponent(uint32_t b, uint32_t ceil_mask) {
+  return (b >> 23) + (((b & 0x7FFFFFu) > 0x600000u ? 1u : 0u) & ceil_mask);
+}
+
 __device__ __forceinline__ void bar_sync_cta(int threads) {
   asm volatile("bar.sync 1, %0;" :: "r"(threads) : "memory");
 }
@@ -337,6 +353,7 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   }
   __syncthreads();
 
+  const uint32_t ceil_mask = a.scale_ceil ? 0xFFFFFFFFu : 0u;   // scale rule
   const int nmb = a.M / 32;    // colwise scale bytes per column
   const int nkb = a.K / 32;    // rowwise scale bytes per row
 
@@ -381,11 +398,11 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                      absmax_bf16x2(xr[i + di][2], xr[i + di][3]));
             }
             // low halves: even columns, high halves: odd columns; fold per row.
-            re[i / 2] = bf16_exponents(
-                absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)));
+            re[i / 2] = bf16_scale_exponents(
+                absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)), ceil_mask);
           }
 #pragma unroll
-          for (int p = 0; p < 4; ++p) ce[p] = bf16_exponents(cm[p]);
+          for (int p = 0; p < 4; ++p) ce[p] = bf16_scale_exponents(cm[p], ceil_mask);
         } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -422,9 +439,13 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
           }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) re[q] = (rmx[2 * q] >> 23) | ((rmx[2 * q + 1] >> 23) << 16);
+          for (int q = 0; q < 4; ++q)
+            re[q] = f32_scale_exponent(rmx[2 * q], ceil_mask) |
+                    (f32_scale_exponent(rmx[2 * q + 1], ceil_mask) << 16);
 #pragma unroll
-          for (int p = 0; p < 4; ++p) ce[p] = (cmx[2 * p] >> 23) | ((cmx[2 * p + 1] >> 23) << 16);
+          for (int p = 0; p < 4; ++p)
+            ce[p] = f32_scale_exponent(cmx[2 * p], ceil_mask) |
+                    (f32_scale_exponent(cmx[2 * p + 1], ceil_mask) << 16);
         }
       }
       // Column maxima over the warp's 16 rows, published for the partner warp

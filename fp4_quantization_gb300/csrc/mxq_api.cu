@@ -181,7 +181,7 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                               float* dbias, void* workspace, size_t workspace_bytes,
                               uint32_t* dev_err, mxq_stream_t stream) {
-  const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH;
+  const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH | MXQ_SCALE_RCEIL;
   if (flags & ~known) return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if ((flags & MXQ_DBIAS) && (flags & MXQ_ACT_GELU_TANH)) return MXQ_EINVAL;
@@ -208,6 +208,7 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_GELU : mxq::ACT_NONE;
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
+  a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.tiles_m = static_cast<int>((M + band - 1) / band);
@@ -247,7 +248,8 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
 mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, uint32_t flags,
                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                              uint32_t* dev_err, mxq_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU))
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU |
+                                     MXQ_SCALE_RCEIL))
     return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if ((flags & MXQ_ACT_GELU_TANH) && (flags & MXQ_ACT_SILU)) return MXQ_EINVAL;
@@ -267,6 +269,7 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
   const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_GEGLU : mxq::ACT_SWIGLU;
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
+  a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(N);
   a.kin = static_cast<int>(N);
@@ -302,7 +305,8 @@ mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t 
                             int64_t ldx, uint32_t flags, uint8_t* q_row, uint8_t* s_row,
                             uint8_t* q_col, uint8_t* s_col, float* dbias, void* workspace,
                             size_t workspace_bytes, uint32_t* dev_err, mxq_stream_t stream) {
-  const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU;
+  const uint32_t known =
+      MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU | MXQ_SCALE_RCEIL;
   if (flags & ~known) return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   const bool gelu = (flags & MXQ_ACT_GELU_TANH) != 0, silu = (flags & MXQ_ACT_SILU) != 0;
@@ -330,6 +334,7 @@ mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t 
   const int act = gelu ? mxq::ACT_DGELU : mxq::ACT_DSILU;
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
+  a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.kin = static_cast<int>(K);
@@ -371,7 +376,8 @@ mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_
                               int64_t ldx, uint32_t flags, uint8_t* q_row, uint8_t* s_row,
                               uint8_t* q_col, uint8_t* s_col, uint32_t* dev_err,
                               mxq_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU))
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU |
+                                     MXQ_SCALE_RCEIL))
     return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if ((flags & MXQ_ACT_GELU_TANH) && (flags & MXQ_ACT_SILU)) return MXQ_EINVAL;
@@ -391,6 +397,7 @@ mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_
   const int act = (flags & MXQ_ACT_GELU_TANH) ? mxq::ACT_DGEGLU : mxq::ACT_DSWIGLU;
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
+  a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(2 * N);       // output width
   a.kin = static_cast<int>(N);

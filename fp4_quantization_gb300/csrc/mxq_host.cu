@@ -93,7 +93,7 @@ extern "C" mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t 
                                               uint32_t flags, uint8_t* q_row, uint8_t* s_row,
                                               uint8_t* q_col, uint8_t* s_col, void* workspace,
                                               size_t workspace_bytes, mxq_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE)) return MXQ_EINVAL;
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SCALE_RCEIL)) return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if (M < 0 || K < 0 || ldx < K) return MXQ_ESHAPE;
   if ((M % 32) || (K % 32)) return MXQ_ESHAPE;

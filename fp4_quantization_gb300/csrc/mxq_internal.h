@@ -33,6 +33,7 @@ struct MxArgs {
   int tiles_m, tiles_k;     // bands of mx_band_rows() rows, 128-column steps over kin
   int up_col;               // column of the second operand in x2 (gated: N; else 0)
   int up_col2;              // column of the third operand in x2 (gated backward: N)
+  int scale_ceil;           // 1: ceil-style E8M0 rule (MXQ_SCALE_RCEIL); 0: floor rule
   uint8_t* q_row;
   uint8_t* s_row;
   uint8_t* q_col;

@@ -74,8 +74,9 @@ enum {
                             /* gate (mx_quantize_gated: GeGLU), its         */
                             /* derivative (mx_quantize_dact / _dgated)     */
     MXQ_NVFP4_2D = 16,      /* 16x16 blocks (nvfp4_quantize_transpose)     */
-    MXQ_ACT_SILU = 32       /* silu: SwiGLU gate (the default of the gated */
+    MXQ_ACT_SILU = 32,      /* silu: SwiGLU gate (the default of the gated */
                             /* calls), its derivative (mx_quantize_dact)   */
+    MXQ_SCALE_RCEIL = 64    /* MXFP8 calls: ceil-style E8M0 rule, below    */
 };
 
 /* bits of *dev_err */
@@ -99,7 +100,10 @@ MXQ_API size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags)
  * with MXQ_ACT_GELU_TANH, gelu_tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi)
  * (x + 0.044715 x^3)))):  a = max|y| over B;  e = floor(log2 a) - 8 clamped
  * to [-127, 127] (a = 0 -> scale code 0);  scale code = e + 127 (E8M0);
- * codes = E4M3(y * 2^-e), round-to-nearest-even, saturating to +-448.  The
+ * codes = E4M3(y * 2^-e), round-to-nearest-even, saturating to +-448.
+ * With MXQ_SCALE_RCEIL (any MXFP8 call) e = ceil(log2(a / 448)) instead,
+ * clamped the same way: the smallest power of two for which no element
+ * exceeds 448, so nothing saturates.  The
  * multiply by the exact power of two 2^-e replaces a per-element division
  * (torchao PR #12, rationale section).  Rowwise blocks are 1x32 along K,
  * colwise blocks 32x1 along M (TE PR #3291 tables, dir "row"/"col"/"both").

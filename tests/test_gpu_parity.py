@@ -92,6 +92,49 @@ def test_mx_rowcol_host_strided_window():
         assert_equal_bytes(out[key].numpy(), ref[key], f"host window {key}")
 
 
+@pytest.mark.parametrize("name,bits", [("plain_small", synth.plain_small()),
+                                       ("dbias_blocks", synth.dbias(M=512, K=1024, seed=79)),
+                                       ("ragged", synth.rowcol(M=3104, K=2080, seed=80))],
+                         ids=["plain_small", "dbias_blocks", "ragged"])
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+def test_mx_rowcol_rceil(name, bits, flags):
+    """Ceil-style scale rule: bit-exact, including zero, subnormal and
+    outlier blocks."""
+    out = mxq.mx_quantize_rowcol(to_device(bits), flags | mxq.SCALE_RCEIL)
+    ref = oracle.mx_quantize(bits, flags | oracle.SCALE_RCEIL)
+    for key in ref:
+        assert_equal_bytes(host(out[key]), ref[key], f"rceil {name} {key}")
+
+
+def test_mx_rceil_fused_paths():
+    """The ceil rule on dbias (exact codes), GELU, SwiGLU and dGELU
+    (activation tolerance), and the host-buffer path."""
+    bits = synth.dbias(M=320, K=224, seed=81)
+    out = mxq.mx_quantize_rowcol(to_device(bits), BOTH | mxq.DBIAS | mxq.SCALE_RCEIL)
+    ref = oracle.mx_quantize(bits, BOTH | oracle.DBIAS | oracle.SCALE_RCEIL)
+    for key in ("q_row", "s_row", "q_col", "s_col"):
+        assert_equal_bytes(host(out[key]), ref[key], f"rceil dbias {key}")
+    g = synth.gelu(M=256, K=384, seed=82)
+    out = mxq.mx_quantize_rowcol(to_device(g), BOTH | mxq.ACT_GELU_TANH | mxq.SCALE_RCEIL)
+    _check_mx_tol(out, oracle.mx_quantize(g, BOTH | oracle.SCALE_RCEIL, act=oracle.ACT_GELU_TANH),
+                  "rceil gelu")
+    sw = synth.swiglu(M=256, N=352, seed=83)
+    out = mxq.mx_quantize_gated(to_device(sw), BOTH | mxq.SCALE_RCEIL)
+    _check_mx_tol(out, oracle.mx_quantize_gated(sw, 352, flags=BOTH | oracle.SCALE_RCEIL),
+                  "rceil swiglu")
+    gr = synth.gelu(M=256, K=384, seed=84)
+    out = mxq.mx_quantize_dact(to_device(gr), to_device(g), BOTH | mxq.ACT_GELU_TANH | mxq.SCALE_RCEIL)
+    _check_mx_tol(out, oracle.mx_quantize_dact(gr, g, oracle.ACT_GELU_TANH, BOTH | oracle.SCALE_RCEIL),
+                  "rceil dgelu")
+    hb = synth.rowcol(M=2176, K=320, seed=85)
+    xh = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out = mxq.mx_quantize_rowcol_host(xh, BOTH | mxq.SCALE_RCEIL)
+    torch.cuda.synchronize()
+    ref = oracle.mx_quantize(hb, BOTH | oracle.SCALE_RCEIL)
+    for key in ref:
+        assert_equal_bytes(out[key].numpy(), ref[key], f"rceil host {key}")
+
+
 def test_mx_rowcol_strided_input():
     """ldx > K: a column window of a wider matrix."""
     full = synth.rowcol(M=128, K=512, seed=35)
