@@ -186,13 +186,13 @@ def mx_quantize(x, flags=ROWWISE | COLWISE, act=ACT_NONE):
         out["s_col"] = np.empty((K, M // 32), np.uint8)
     if flags & DBIAS:
         out["dbias"] = np.empty(K, np.float32)
-    rc = lib().orc_mx_quantize(p, M, K, ld, flags, act,
+    rc = lib().orc_mx_quantize(p, M, K, ld, flags & ~SCALE_SWIZZLED, act,
                                _u8(out.get("q_row")), _u8(out.get("s_row")),
                                _u8(out.get("q_col")), _u8(out.get("s_col")),
                                _f32(out.get("dbias")))
     if rc != 0:
         raise ValueError(f"orc_mx_quantize rejected M={M} K={K} ld={ld} act={act}")
-    return out
+    return _maybe_swizzle(out, flags)
 
 
 def mx_quantize_swiglu(x, N, up_offset=None, flags=ROWWISE | COLWISE):
@@ -266,12 +266,12 @@ def mx_quantize_gated(x, N, act=ACT_SILU, up_offset=None, flags=ROWWISE | COLWIS
     if up_offset is None:
         up_offset = N
     out = _mx_outputs(M, N, flags & (ROWWISE | COLWISE))
-    rc = lib().orc_mx_quantize_gated(p, M, N, ld, up_offset, flags, act,
+    rc = lib().orc_mx_quantize_gated(p, M, N, ld, up_offset, flags & ~SCALE_SWIZZLED, act,
                                      _u8(out.get("q_row")), _u8(out.get("s_row")),
                                      _u8(out.get("q_col")), _u8(out.get("s_col")))
     if rc != 0:
         raise ValueError(f"orc_mx_quantize_gated rejected M={M} N={N} ld={ld} act={act}")
-    return out
+    return _maybe_swizzle(out, flags)
 
 
 def mx_quantize_dact(grad, x, act, flags=ROWWISE | COLWISE):
@@ -282,13 +282,13 @@ def mx_quantize_dact(grad, x, act, flags=ROWWISE | COLWISE):
     if (M2, K2) != (M, K):
         raise ValueError("grad and x shapes differ")
     out = _mx_outputs(M, K, flags)
-    rc = lib().orc_mx_quantize_dact(pg, px, M, K, ldg, ldx, flags, act,
+    rc = lib().orc_mx_quantize_dact(pg, px, M, K, ldg, ldx, flags & ~SCALE_SWIZZLED, act,
                                     _u8(out.get("q_row")), _u8(out.get("s_row")),
                                     _u8(out.get("q_col")), _u8(out.get("s_col")),
                                     _f32(out.get("dbias")))
     if rc != 0:
         raise ValueError(f"orc_mx_quantize_dact rejected M={M} K={K} act={act}")
-    return out
+    return _maybe_swizzle(out, flags)
 
 
 def mx_quantize_dgated(grad, x, N, act, up_offset=None, flags=ROWWISE | COLWISE):
@@ -301,9 +301,50 @@ def mx_quantize_dgated(grad, x, N, act, up_offset=None, flags=ROWWISE | COLWISE)
     if M2 != M or Ng != N:
         raise ValueError("grad must be [M, N] for x = [gate | up]")
     out = _mx_outputs(M, 2 * N, flags & (ROWWISE | COLWISE))
-    rc = lib().orc_mx_quantize_dgated(pg, px, M, N, ldg, ldx, up_offset, flags, act,
+    rc = lib().orc_mx_quantize_dgated(pg, px, M, N, ldg, ldx, up_offset, flags & ~SCALE_SWIZZLED,
+                                      act,
                                       _u8(out.get("q_row")), _u8(out.get("s_row")),
                                       _u8(out.get("q_col")), _u8(out.get("s_col")))
     if rc != 0:
         raise ValueError(f"orc_mx_quantize_dgated rejected M={M} N={N} act={act}")
+    return _maybe_swizzle(out, flags)
+
+
+# --------------------------------------------------------------------------
+# Tiled scale layout (flag SCALE_SWIZZLED of the MXFP8 calls)
+# --------------------------------------------------------------------------
+
+SCALE_SWIZZLED = 128
+
+
+def _maybe_swizzle(out, flags):
+    if flags & SCALE_SWIZZLED:
+        for key in ("s_row", "s_col"):
+            if key in out:
+                out[key] = swizzle_scales(out[key])
     return out
+
+
+def swizzled_shape(R, C):
+    """Padded [R', C'] of an [R][C] scale matrix in the tiled layout."""
+    return -(-R // 128) * 128, -(-C // 4) * 4
+
+
+def swizzle_scales(s):
+    """[R][C] row-major scale bytes -> the tiled layout block-scaled GEMMs
+    read: padded to R' = ceil(R/128)*128 rows and C' = ceil(C/4)*4 columns
+    (padding 0), cut into 128x4 tiles stored one after another in row-major
+    tile order (tile (i, j) at byte (i * C'/4 + j) * 512); inside a tile,
+    entry (r, c) sits at byte (r % 32) * 16 + (r // 32) * 4 + c.  Returned
+    as an [R', C'] uint8 array holding those bytes in order."""
+    s = np.asarray(s, dtype=np.uint8)
+    R, C = s.shape
+    Rp, Cp = swizzled_shape(R, C)
+    out = np.zeros(Rp * Cp, np.uint8)
+    tiles_c = Cp // 4
+    for r in range(R):
+        i, rr = divmod(r, 128)
+        for c in range(C):
+            j, cc = divmod(c, 4)
+            out[(i * tiles_c + j) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + cc] = s[r, c]
+    return out.reshape(Rp, Cp)

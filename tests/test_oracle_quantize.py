@@ -499,3 +499,34 @@ def test_mx_rceil_blocks_never_saturate():
             assert out["s_col"][k, mb] == code
             np.testing.assert_array_equal(out["q_col"][k, mb * 32:(mb + 1) * 32],
                                           oracle.e4m3_encode(np.ldexp(blk, 127 - int(code))))
+
+
+def test_swizzle_matches_tile_reshape():
+    """The tiled scale layout by its index formula equals the same layout
+    built as a reshape: pad to [R', C'], view as [R'/128][4][32][C'/4][4]
+    (tile row, row // 32 in tile, row % 32, tile column, column in tile) and
+    order the axes (tile row, tile column, row % 32, row // 32, column); also
+    a bijection of the padded positions."""
+    rng = np.random.default_rng(24)
+    for R, C in ((128, 4), (256, 12), (96, 6), (300, 17), (32, 1)):
+        s = rng.integers(1, 255, size=(R, C), dtype=np.uint8)
+        got = oracle.swizzle_scales(s)
+        Rp, Cp = oracle.swizzled_shape(R, C)
+        pad = np.zeros((Rp, Cp), np.uint8)
+        pad[:R, :C] = s
+        want = pad.reshape(Rp // 128, 4, 32, Cp // 4, 4).transpose(0, 3, 2, 1, 4).reshape(Rp, Cp)
+        np.testing.assert_array_equal(got, want)
+        idx = np.arange(Rp * Cp).reshape(Rp, Cp) % 251 + 1
+        assert np.array_equal(np.sort(oracle.swizzle_scales(idx.astype(np.uint8)).ravel()),
+                              np.sort(idx.astype(np.uint8).ravel()))
+
+
+def test_swizzled_quantize_is_the_row_major_result_retiled():
+    x = synth.dbias(M=160, K=288, seed=25)
+    plain = oracle.mx_quantize(x, 3)
+    swz = oracle.mx_quantize(x, 3 | oracle.SCALE_SWIZZLED)
+    np.testing.assert_array_equal(swz["q_row"], plain["q_row"])
+    np.testing.assert_array_equal(swz["q_col"], plain["q_col"])
+    np.testing.assert_array_equal(swz["s_row"], oracle.swizzle_scales(plain["s_row"]))
+    np.testing.assert_array_equal(swz["s_col"], oracle.swizzle_scales(plain["s_col"]))
+    assert swz["s_row"].shape == (256, 12) and swz["s_col"].shape == (384, 8)
