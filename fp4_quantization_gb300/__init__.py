@@ -21,6 +21,15 @@ ACT_GELU_TANH = 8
 NVFP4_2D = 16
 ACT_SILU = 32
 SCALE_RCEIL = 64
+SCALE_SWIZZLED = 128
+
+
+def scale_shape(R, C, flags):
+    """Shape of an [R][C] scale matrix as written under `flags`: padded to
+    128 x 4 tiles with SCALE_SWIZZLED, else [R, C]."""
+    if flags & SCALE_SWIZZLED:
+        return (-(-R // 128) * 128, -(-C // 4) * 4)
+    return (R, C)
 OP_ROWCOL = 0
 OP_NVFP4 = 1
 OP_DACT = 2
@@ -85,10 +94,12 @@ def mx_quantize_rowcol(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_
     out = {}
     if flags & ROWWISE:
         out["q_row"] = q_row if q_row is not None else _empty((M, K), torch.uint8, dev)
-        out["s_row"] = s_row if s_row is not None else _empty((M, K // 32), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty(scale_shape(M, K // 32, flags),
+                                                              torch.uint8, dev)
     if flags & COLWISE:
         out["q_col"] = q_col if q_col is not None else _empty((K, M), torch.uint8, dev)
-        out["s_col"] = s_col if s_col is not None else _empty((K, M // 32), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty(scale_shape(K, M // 32, flags),
+                                                              torch.uint8, dev)
     ws_bytes = 0
     if flags & DBIAS:
         out["dbias"] = dbias if dbias is not None else _empty((K,), torch.float32, dev)
@@ -118,10 +129,12 @@ def mx_quantize_rowcol_dbias_noalloc(x, flags=ROWWISE | COLWISE, *, q_row=None, 
     out = {}
     if flags & ROWWISE:
         out["q_row"] = q_row if q_row is not None else _empty((M, K), torch.uint8, dev)
-        out["s_row"] = s_row if s_row is not None else _empty((M, K // 32), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty(scale_shape(M, K // 32, flags),
+                                                              torch.uint8, dev)
     if flags & COLWISE:
         out["q_col"] = q_col if q_col is not None else _empty((K, M), torch.uint8, dev)
-        out["s_col"] = s_col if s_col is not None else _empty((K, M // 32), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty(scale_shape(K, M // 32, flags),
+                                                              torch.uint8, dev)
     out["dbias"] = dbias if dbias is not None else _empty((K,), torch.float32, dev)
     st = _lib.lib().mx_quantize_rowcol_dbias_noalloc(
         _ptr(x), M, K, ldx, flags, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
@@ -152,10 +165,10 @@ def mx_quantize_rowcol_host(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=Non
     out = {}
     if flags & ROWWISE:
         out["q_row"] = host((M, K), q_row)
-        out["s_row"] = host((M, K // 32), s_row)
+        out["s_row"] = host(scale_shape(M, K // 32, flags), s_row)
     if flags & COLWISE:
         out["q_col"] = host((K, M), q_col)
-        out["s_col"] = host((K, M // 32), s_col)
+        out["s_col"] = host(scale_shape(K, M // 32, flags), s_col)
     if workspace is None:
         need = mxq_workspace_bytes(OP_ROWCOL_HOST, M, K, flags)
         workspace = _empty((max(need, 256),), torch.uint8, torch.device("cuda"))
@@ -181,10 +194,12 @@ def mx_quantize_gated(x, flags=ROWWISE | COLWISE, *, q_row=None, s_row=None, q_c
     out = {}
     if flags & ROWWISE:
         out["q_row"] = q_row if q_row is not None else _empty((M, N), torch.uint8, dev)
-        out["s_row"] = s_row if s_row is not None else _empty((M, N // 32), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty(scale_shape(M, N // 32, flags),
+                                                              torch.uint8, dev)
     if flags & COLWISE:
         out["q_col"] = q_col if q_col is not None else _empty((N, M), torch.uint8, dev)
-        out["s_col"] = s_col if s_col is not None else _empty((N, M // 32), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty(scale_shape(N, M // 32, flags),
+                                                              torch.uint8, dev)
     st = _lib.lib().mx_quantize_gated(
         _ptr(x), M, N, ldx, flags, _ptr(out.get("q_row")), _ptr(out.get("s_row")),
         _ptr(out.get("q_col")), _ptr(out.get("s_col")), _ptr(dev_err), _stream(stream))
@@ -196,10 +211,12 @@ def _mx_outputs(M, K, flags, dev, q_row, s_row, q_col, s_col):
     out = {}
     if flags & ROWWISE:
         out["q_row"] = q_row if q_row is not None else _empty((M, K), torch.uint8, dev)
-        out["s_row"] = s_row if s_row is not None else _empty((M, K // 32), torch.uint8, dev)
+        out["s_row"] = s_row if s_row is not None else _empty(scale_shape(M, K // 32, flags),
+                                                              torch.uint8, dev)
     if flags & COLWISE:
         out["q_col"] = q_col if q_col is not None else _empty((K, M), torch.uint8, dev)
-        out["s_col"] = s_col if s_col is not None else _empty((K, M // 32), torch.uint8, dev)
+        out["s_col"] = s_col if s_col is not None else _empty(scale_shape(K, M // 32, flags),
+                                                              torch.uint8, dev)
     return out
 
 

@@ -17,7 +17,17 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmxq.so")
 
-SOURCES = ["mxq_api.cu", "mx_kernels.cu", "nvfp4_kernels.cu", "mxq_noalloc.cu", "mxq_host.cu"]
+# (source, extra nvcc flags, object): mx_kernels.cu is built twice, for the
+# row-major and the tiled scale layouts.
+UNITS = [
+    ("mxq_api.cu", [], "mxq_api.o"),
+    ("mx_kernels.cu", [], "mx_kernels.o"),
+    ("mx_kernels.cu", ["-DMXQ_TILED_SCALES=1"], "mx_kernels_tiled.o"),
+    ("nvfp4_kernels.cu", [], "nvfp4_kernels.o"),
+    ("mxq_noalloc.cu", [], "mxq_noalloc.o"),
+    ("mxq_host.cu", [], "mxq_host.o"),
+]
+SOURCES = sorted({src for src, _, _ in UNITS})
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -54,16 +64,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     # Optional -D overrides of the launch configuration (tuning builds).
     extra += os.environ.get("MXQ_NVCC_DEFINES", "").split()
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(unit):
+        src, flags, obj_name = unit
+        obj = os.path.join(BUILD_DIR, obj_name)
+        cmd = [nvcc, *NVCC_FLAGS, *flags, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stdout + r.stderr
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
-        results = list(pool.map(compile_one, SOURCES))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(UNITS)) as pool:
+        results = list(pool.map(compile_one, UNITS))
     if verbose or ptxas_verbose:
         for _, log in results:
             if log.strip():

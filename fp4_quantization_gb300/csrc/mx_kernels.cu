@@ -49,6 +49,14 @@
 #include "mxq_internal.h"
 #include "mxq_ptx.cuh"
 
+// This file is compiled twice: with MXQ_TILED_SCALES 0 (row-major scale
+// output; exports launch_mx and the shared helpers) and 1 (scales in 128 x 4
+// tiles; exports launch_mx_tiled), so neither variant carries the other's
+// scale code.
+#ifndef MXQ_TILED_SCALES
+#define MXQ_TILED_SCALES 0
+#endif
+
 namespace mxq {
 namespace {
 
@@ -639,7 +647,33 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
           const int fb = (pos.g == p0.g && tk == p0.tk) ? p0.bi : 0;   // first band staged
           const int mb0 = (pos.g * GROUP + fb) * L::BPB;     // its first block along m
           const int nblk = min((pos.bi + 1 - fb) * L::BPB, nmb - mb0);
-          if (nblk == NB && (nmb % CH) == 0) {
+          if constexpr (MXQ_TILED_SCALES) {
+            // Tiled layout: band bb's 4 blocks of the step's 128 columns are
+            // the 128 x 4 tile (k / 128, band); lane L writes its 16 bytes,
+            // columns L, L + 32, L + 64, L + 96 (4 blocks each).
+            static_assert(L::BPB == 4, "one 128 x 4 tile per band and step");
+            const int tiles_m = (nmb + 3) / 4;
+            const int ktile = (obase >> 7) + tk;
+            for (int it = tid; it < (pos.bi + 1 - fb) * 32; it += THREADS) {
+              const int bb = fb + (it >> 5), ln = it & 31;
+              uint32_t w[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int kc = ln + 32 * q;
+                if constexpr (L::CSC_BY_COL) {
+                  w[q] = lds32(sbase + L::OFF_CSC + L::csc(0, kc));
+                } else {
+                  w[q] = 0u;
+#pragma unroll
+                  for (int cb = 0; cb < 4; ++cb)
+                    w[q] |= ld_shared_u8(sbase + L::OFF_CSC + L::csc(bb * 4 + cb, kc)) << (8 * cb);
+                }
+              }
+              uint8_t* dst = a.s_col +
+                             (static_cast<size_t>(ktile) * tiles_m + pos.g * GROUP + bb) * 512 + 16 * ln;
+              stg128(dst, w[0], w[1], w[2], w[3]);
+            }
+          } else if (nblk == NB && (nmb % CH) == 0) {
             // Item i = (chunk, column); warp w takes items w * IPW .. + IPW - 1.
             constexpr int ITEMS = MX_TILE_K * (NB / CH);
             constexpr int IPW = ITEMS / WARPS;
@@ -679,7 +713,18 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
       if constexpr (ROW) {
         // This band's next step in this CTA, if any, is j + nb.
         const bool flush = (slot == 7) || (tk + 1 == a.tiles_k) || (j + pos.nb >= count);
-        if (flush) {
+        if constexpr (MXQ_TILED_SCALES) {
+          // Tiled layout: the step's 4 blocks of the band's 128 rows are the
+          // 128 x 4 tile (band, column / 128), written every step by one warp:
+          // lane L holds rows L, L + 32, L + 64, L + 96 (4 blocks each).
+          if (warp == WARPS - 1) {
+            const int tiles_k = (nkb + 3) / 4;
+            const uint32_t src = sbase + L::OFF_RSC + ((t * GROUP + pos.bi) * BAND + lane) * 32 + slot * 4;
+            uint8_t* dst = a.s_row +
+                           (static_cast<size_t>(band) * tiles_k + (obase >> 7) + tk) * 512 + 16 * lane;
+            stg128(dst, lds32(src), lds32(src + 32 * 32), lds32(src + 64 * 32), lds32(src + 96 * 32));
+          }
+        } else if (flush) {
           // Rowwise scale bytes of steps rsc_first..slot of this group of eight
           // (the CTA's first step for this band may fall inside the group):
           // one 32-byte sector per row when all eight steps are present,
@@ -931,6 +976,10 @@ cudaError_t launch_mode(const MxMaps& maps, const MxArgs& a, int mode, int num_s
 
 }  // namespace
 
+#if MXQ_TILED_SCALES
+#define MXQ_LAUNCH_NAME launch_mx_tiled
+#else
+#define MXQ_LAUNCH_NAME launch_mx
 int mx_band_rows(int act) {
   switch (act) {
     case ACT_GELU: return 16 * MxConfig<ACT_GELU>::WARPS;
@@ -944,7 +993,16 @@ int mx_band_rows(int act) {
   }
 }
 
-cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
+cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
+                                  cudaStream_t stream) {
+  const int blocks = (K + kFinalizeCols - 1) / kFinalizeCols;
+  dbias_finalize_kernel<<<blocks, 4 * kFinalizeCols, 0, stream>>>(ws, bands, K, dbias);
+  return cudaGetLastError();
+}
+
+#endif
+
+cudaError_t MXQ_LAUNCH_NAME(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
                       int num_sms, cudaStream_t stream) {
   if (dbias) {
     switch (act) {
@@ -963,13 +1021,6 @@ cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias,
     case ACT_DGEGLU: return launch_mode<false, ACT_DGEGLU>(maps, a, mode, num_sms, stream);
     default: return launch_mode<false, ACT_NONE>(maps, a, mode, num_sms, stream);
   }
-}
-
-cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
-                                  cudaStream_t stream) {
-  const int blocks = (K + kFinalizeCols - 1) / kFinalizeCols;
-  dbias_finalize_kernel<<<blocks, 4 * kFinalizeCols, 0, stream>>>(ws, bands, K, dbias);
-  return cudaGetLastError();
 }
 
 }  // namespace mxq

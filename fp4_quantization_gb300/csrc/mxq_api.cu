@@ -146,6 +146,13 @@ mxq_status check_mx_outputs(uint32_t flags, int64_t width, const uint8_t* q_row,
   return MXQ_OK;
 }
 
+// The MXFP8 kernels built for the call's scale layout.
+cudaError_t launch_mx_for(const mxq::MxMaps& maps, const mxq::MxArgs& a, int mode, bool dbias,
+                          int act, int num_sms, cudaStream_t stream) {
+  return a.scale_tiled ? mxq::launch_mx_tiled(maps, a, mode, dbias, act, num_sms, stream)
+                       : mxq::launch_mx(maps, a, mode, dbias, act, num_sms, stream);
+}
+
 int direction_mode(uint32_t flags) {
   return ((flags & MXQ_ROWWISE) ? mxq::MX_ROW : 0) | ((flags & MXQ_COLWISE) ? mxq::MX_COL : 0);
 }
@@ -181,7 +188,8 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                               float* dbias, void* workspace, size_t workspace_bytes,
                               uint32_t* dev_err, mxq_stream_t stream) {
-  const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH | MXQ_SCALE_RCEIL;
+  const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH |
+                         MXQ_SCALE_RCEIL | MXQ_SCALE_SWIZZLED;
   if (flags & ~known) return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if ((flags & MXQ_DBIAS) && (flags & MXQ_ACT_GELU_TANH)) return MXQ_EINVAL;
@@ -209,6 +217,7 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
   a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
+  a.scale_tiled = (flags & MXQ_SCALE_SWIZZLED) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.tiles_m = static_cast<int>((M + band - 1) / band);
@@ -240,7 +249,7 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
     if (st != MXQ_OK) return st;
   }
   maps.q_row2 = maps.q_row;
-  st = from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
+  st = from_cuda(launch_mx_for(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
   if (st != MXQ_OK || !want_dbias) return st;
   return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
 }
@@ -249,7 +258,7 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                              uint32_t* dev_err, mxq_stream_t stream) {
   if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU |
-                                     MXQ_SCALE_RCEIL))
+                                     MXQ_SCALE_RCEIL | MXQ_SCALE_SWIZZLED))
     return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if ((flags & MXQ_ACT_GELU_TANH) && (flags & MXQ_ACT_SILU)) return MXQ_EINVAL;
@@ -270,6 +279,7 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
   a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
+  a.scale_tiled = (flags & MXQ_SCALE_SWIZZLED) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(N);
   a.kin = static_cast<int>(N);
@@ -298,7 +308,7 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
     if (st != MXQ_OK) return st;
   }
   maps.q_row2 = maps.q_row;
-  return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, act, sms, stream));
+  return from_cuda(launch_mx_for(maps, a, direction_mode(flags), false, act, sms, stream));
 }
 
 mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t K, int64_t ldg,
@@ -306,7 +316,8 @@ mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t 
                             uint8_t* q_col, uint8_t* s_col, float* dbias, void* workspace,
                             size_t workspace_bytes, uint32_t* dev_err, mxq_stream_t stream) {
   const uint32_t known =
-      MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU | MXQ_SCALE_RCEIL;
+      MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU | MXQ_SCALE_RCEIL |
+      MXQ_SCALE_SWIZZLED;
   if (flags & ~known) return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   const bool gelu = (flags & MXQ_ACT_GELU_TANH) != 0, silu = (flags & MXQ_ACT_SILU) != 0;
@@ -335,6 +346,7 @@ mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t 
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
   a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
+  a.scale_tiled = (flags & MXQ_SCALE_SWIZZLED) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.kin = static_cast<int>(K);
@@ -367,7 +379,7 @@ mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t 
     if (st != MXQ_OK) return st;
   }
   maps.q_row2 = maps.q_row;
-  st = from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
+  st = from_cuda(launch_mx_for(maps, a, direction_mode(flags), want_dbias, act, sms, stream));
   if (st != MXQ_OK || !want_dbias) return st;
   return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
 }
@@ -377,12 +389,14 @@ mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_
                               uint8_t* q_col, uint8_t* s_col, uint32_t* dev_err,
                               mxq_stream_t stream) {
   if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_ACT_GELU_TANH | MXQ_ACT_SILU |
-                                     MXQ_SCALE_RCEIL))
+                                     MXQ_SCALE_RCEIL | MXQ_SCALE_SWIZZLED))
     return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if ((flags & MXQ_ACT_GELU_TANH) && (flags & MXQ_ACT_SILU)) return MXQ_EINVAL;
   if (M < 0 || N < 0 || ldg < N || ldx < 2 * N) return MXQ_ESHAPE;
   if ((M % 32) || (N % 32)) return MXQ_ESHAPE;
+  // Tiled scales: the d-up half must start on a 128-column tile boundary.
+  if ((flags & MXQ_SCALE_SWIZZLED) && (N % 128)) return MXQ_ESHAPE;
   if (M > (int64_t(1) << 30) || N > (int64_t(1) << 29) || M * N > (int64_t(1) << 39))
     return MXQ_ESHAPE;
   int sms = 0;
@@ -398,6 +412,7 @@ mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_
   const int band = mxq::mx_band_rows(act);
   mxq::MxArgs a{};
   a.scale_ceil = (flags & MXQ_SCALE_RCEIL) != 0;
+  a.scale_tiled = (flags & MXQ_SCALE_SWIZZLED) != 0;
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(2 * N);       // output width
   a.kin = static_cast<int>(N);
@@ -432,7 +447,7 @@ mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_
     st = encode_mx_qrow_map(&maps.q_row2, q_row + N, M, N, 2 * N, band);
     if (st != MXQ_OK) return st;
   }
-  return from_cuda(mxq::launch_mx(maps, a, direction_mode(flags), false, act, sms, stream));
+  return from_cuda(launch_mx_for(maps, a, direction_mode(flags), false, act, sms, stream));
 }
 
 mxq_status bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* amax_out,

@@ -63,6 +63,7 @@ mxq_status pipe_on_current_device(HostPipe** out) {
 }
 
 int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Device bytes of one panel's buffers: input, codes and scales of both
 // directions, and the workspace mx_quantize_rowcol needs (none without dbias).
@@ -72,9 +73,10 @@ struct PanelLayout {
     x = 0;
     q_row = x + round256(P * K * 2);
     s_row = q_row + round256(P * K);
-    q_col = s_row + round256(P * K / 32);
+    // Scale buffers sized for the tiled layout too (128 x 4 tiles, padded).
+    q_col = s_row + round256(ceil_div(P, 128) * 128 * ceil_div(K / 32, 4) * 4);
     s_col = q_col + round256(K * P);
-    bytes = s_col + round256(K * P / 32);
+    bytes = s_col + round256(ceil_div(K, 128) * 128 * ceil_div(P / 32, 4) * 4);
   }
 };
 
@@ -93,7 +95,8 @@ extern "C" mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t 
                                               uint32_t flags, uint8_t* q_row, uint8_t* s_row,
                                               uint8_t* q_col, uint8_t* s_col, void* workspace,
                                               size_t workspace_bytes, mxq_stream_t stream) {
-  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SCALE_RCEIL)) return MXQ_EINVAL;
+  if (flags & ~static_cast<uint32_t>(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SCALE_RCEIL | MXQ_SCALE_SWIZZLED))
+    return MXQ_EINVAL;
   if (!(flags & (MXQ_ROWWISE | MXQ_COLWISE))) return MXQ_EINVAL;
   if (M < 0 || K < 0 || ldx < K) return MXQ_ESHAPE;
   if ((M % 32) || (K % 32)) return MXQ_ESHAPE;
@@ -114,6 +117,9 @@ extern "C" mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t 
   const PanelLayout L(P, K);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const bool row = (flags & MXQ_ROWWISE) != 0, col = (flags & MXQ_COLWISE) != 0;
+  const bool tiled = (flags & MXQ_SCALE_SWIZZLED) != 0;
+  const int64_t tiles_k = ceil_div(K / 32, 4);   // tile columns of the rowwise scales
+  const int64_t tiles_m = ceil_div(M, 128);      // tile columns of the colwise scales
   auto cu = [](cudaError_t e) { return e == cudaSuccess ? MXQ_OK : MXQ_ECUDA; };
 
   // Everything below runs after the work already queued on `stream`.
@@ -146,17 +152,25 @@ extern "C" mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t 
     if (row) {
       st = cu(cudaMemcpyAsync(q_row + m0 * K, buf + L.q_row, rows * K, cudaMemcpyDeviceToHost,
                               p->d2h));
+      // Tiled rowwise scales: the panel's tile rows are contiguous in both.
       if (st == MXQ_OK)
-        st = cu(cudaMemcpyAsync(s_row + m0 * (K / 32), buf + L.s_row, rows * (K / 32),
-                                cudaMemcpyDeviceToHost, p->d2h));
+        st = tiled ? cu(cudaMemcpyAsync(s_row + (m0 / 128) * tiles_k * 512, buf + L.s_row,
+                                        ceil_div(rows, 128) * tiles_k * 512,
+                                        cudaMemcpyDeviceToHost, p->d2h))
+                   : cu(cudaMemcpyAsync(s_row + m0 * (K / 32), buf + L.s_row, rows * (K / 32),
+                                        cudaMemcpyDeviceToHost, p->d2h));
       if (st != MXQ_OK) return st;
     }
     if (col) {
       st = cu(cudaMemcpy2DAsync(q_col + m0, M, buf + L.q_col, rows, rows, K,
                                 cudaMemcpyDeviceToHost, p->d2h));
+      // Tiled colwise scales: the panel's tiles of every tile row.
       if (st == MXQ_OK)
-        st = cu(cudaMemcpy2DAsync(s_col + m0 / 32, M / 32, buf + L.s_col, rows / 32, rows / 32, K,
-                                  cudaMemcpyDeviceToHost, p->d2h));
+        st = tiled ? cu(cudaMemcpy2DAsync(s_col + (m0 / 128) * 512, tiles_m * 512, buf + L.s_col,
+                                          ceil_div(rows, 128) * 512, ceil_div(rows, 128) * 512,
+                                          ceil_div(K, 128), cudaMemcpyDeviceToHost, p->d2h))
+                   : cu(cudaMemcpy2DAsync(s_col + m0 / 32, M / 32, buf + L.s_col, rows / 32,
+                                          rows / 32, K, cudaMemcpyDeviceToHost, p->d2h));
       if (st != MXQ_OK) return st;
     }
     if ((st = cu(cudaEventRecord(p->freed[b], p->d2h))) != MXQ_OK) return st;

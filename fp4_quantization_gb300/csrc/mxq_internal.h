@@ -34,6 +34,7 @@ struct MxArgs {
   int up_col;               // column of the second operand in x2 (gated: N; else 0)
   int up_col2;              // column of the third operand in x2 (gated backward: N)
   int scale_ceil;           // 1: ceil-style E8M0 rule (MXQ_SCALE_RCEIL); 0: floor rule
+  int scale_tiled;          // 1: scales in 128 x 4 tiles (MXQ_SCALE_SWIZZLED); 0: row-major
   uint8_t* q_row;
   uint8_t* s_row;
   uint8_t* q_col;
@@ -88,6 +89,9 @@ int mx_band_rows(int act);
 
 cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
                       int num_sms, cudaStream_t stream);
+// The same kernels built to write the scales in 128 x 4 tiles (a.scale_tiled).
+cudaError_t launch_mx_tiled(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
+                            int num_sms, cudaStream_t stream);
 cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
                                   cudaStream_t stream);
 int nv_band_rows();

@@ -76,7 +76,8 @@ enum {
     MXQ_NVFP4_2D = 16,      /* 16x16 blocks (nvfp4_quantize_transpose)     */
     MXQ_ACT_SILU = 32,      /* silu: SwiGLU gate (the default of the gated */
                             /* calls), its derivative (mx_quantize_dact)   */
-    MXQ_SCALE_RCEIL = 64    /* MXFP8 calls: ceil-style E8M0 rule, below    */
+    MXQ_SCALE_RCEIL = 64,   /* MXFP8 calls: ceil-style E8M0 rule, below    */
+    MXQ_SCALE_SWIZZLED = 128 /* MXFP8 calls: scales in 128x4 tiles, below   */
 };
 
 /* bits of *dev_err */
@@ -103,7 +104,15 @@ MXQ_API size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags)
  * codes = E4M3(y * 2^-e), round-to-nearest-even, saturating to +-448.
  * With MXQ_SCALE_RCEIL (any MXFP8 call) e = ceil(log2(a / 448)) instead,
  * clamped the same way: the smallest power of two for which no element
- * exceeds 448, so nothing saturates.  The
+ * exceeds 448, so nothing saturates.
+ * With MXQ_SCALE_SWIZZLED (any MXFP8 call) each scale matrix [R][C] (R = M,
+ * C = K/32 rowwise; R = K, C = M/32 colwise) is written in the tiled layout
+ * block-scaled GEMMs read instead of row-major: padded to R' =
+ * ceil(R/128)*128 rows and C' = ceil(C/4)*4 columns (padding bytes 0), cut
+ * into 128x4 tiles stored one after another in row-major tile order (tile
+ * (i, j) at byte (i * C'/4 + j) * 512); inside a tile, entry (r, c) is at
+ * byte (r % 32) * 16 + (r / 32) * 4 + c.  The buffers must hold R' * C'
+ * bytes.  (mx_quantize_dgated additionally needs N % 128 == 0.)  The
  * multiply by the exact power of two 2^-e replaces a per-element division
  * (torchao PR #12, rationale section).  Rowwise blocks are 1x32 along K,
  * colwise blocks 32x1 along M (TE PR #3291 tables, dir "row"/"col"/"both").

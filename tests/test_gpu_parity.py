@@ -135,6 +135,60 @@ def test_mx_rceil_fused_paths():
         assert_equal_bytes(out[key].numpy(), ref[key], f"rceil host {key}")
 
 
+def _untile(t, R, C):
+    """Inverse of the 128 x 4 tiled scale layout (reshape form), cropped to
+    [R, C]."""
+    t = np.asarray(t)
+    Rp, Cp = t.shape
+    return t.reshape(Rp // 128, Cp // 4, 32, 4, 4).transpose(0, 3, 2, 1, 4).reshape(Rp, Cp)[:R, :C]
+
+
+@pytest.mark.parametrize("name,bits", [("plain_small", synth.plain_small()),
+                                       ("ragged", synth.rowcol(M=3104, K=2080, seed=86)),
+                                       ("whole_groups", synth.dim1(M=8192, K=1024, seed=87))],
+                         ids=["plain_small", "ragged", "whole_groups"])
+@pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
+def test_mx_rowcol_tiled_scales(name, bits, flags):
+    """Scales in the 128 x 4 tiled layout, padding included, byte for byte."""
+    out = mxq.mx_quantize_rowcol(to_device(bits), flags | mxq.SCALE_SWIZZLED)
+    ref = oracle.mx_quantize(bits, flags | oracle.SCALE_SWIZZLED)
+    for key in ref:
+        assert_equal_bytes(host(out[key]), ref[key], f"tiled {name} {key}")
+
+
+def test_mx_tiled_scales_fused_paths():
+    bits = synth.dbias(M=320, K=224, seed=88)
+    out = mxq.mx_quantize_rowcol(to_device(bits), BOTH | mxq.DBIAS | mxq.SCALE_SWIZZLED)
+    ref = oracle.mx_quantize(bits, BOTH | oracle.DBIAS | oracle.SCALE_SWIZZLED)
+    for key in ("q_row", "s_row", "q_col", "s_col"):
+        assert_equal_bytes(host(out[key]), ref[key], f"tiled dbias {key}")
+    g = synth.gelu(M=256, K=384, seed=89)
+    out = mxq.mx_quantize_rowcol(to_device(g), BOTH | mxq.ACT_GELU_TANH | mxq.SCALE_SWIZZLED)
+    ref = oracle.mx_quantize(g, BOTH, act=oracle.ACT_GELU_TANH)
+    check_activation_blocks(host(out["q_row"]), _untile(host(out["s_row"]), 256, 12), ref["q_row"],
+                            ref["s_row"], 1, "tiled gelu row")
+    check_activation_blocks(host(out["q_col"]), _untile(host(out["s_col"]), 384, 8), ref["q_col"],
+                            ref["s_col"], 1, "tiled gelu col")
+    x = synth.swiglu(M=256, N=256, seed=90)
+    grad = synth.gelu(M=256, K=256, seed=91)
+    out = mxq.mx_quantize_dgated(to_device(grad), to_device(x), BOTH | mxq.SCALE_SWIZZLED)
+    ref = oracle.mx_quantize_dgated(grad, x, 256, oracle.ACT_SILU)
+    check_activation_blocks(host(out["q_row"]), _untile(host(out["s_row"]), 256, 16), ref["q_row"],
+                            ref["s_row"], 1, "tiled dswiglu row")
+    check_activation_blocks(host(out["q_col"]), _untile(host(out["s_col"]), 512, 8), ref["q_col"],
+                            ref["s_col"], 1, "tiled dswiglu col")
+    with pytest.raises(mxq.MxqError):
+        mxq.mx_quantize_dgated(to_device(synth.gelu(M=64, K=96, seed=92)),
+                               to_device(synth.swiglu(M=64, N=96, seed=93)), BOTH | mxq.SCALE_SWIZZLED)
+    hb = synth.rowcol(M=4192, K=1056, seed=94)
+    xh = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out = mxq.mx_quantize_rowcol_host(xh, BOTH | mxq.SCALE_SWIZZLED)
+    torch.cuda.synchronize()
+    ref = oracle.mx_quantize(hb, BOTH | oracle.SCALE_SWIZZLED)
+    for key in ref:
+        assert_equal_bytes(out[key].numpy(), ref[key], f"tiled host {key}")
+
+
 def test_mx_rowcol_strided_input():
     """ldx > K: a column window of a wider matrix."""
     full = synth.rowcol(M=128, K=512, seed=35)
