@@ -254,6 +254,10 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
     named `only` when given)."""
     out = {}
     cases = [
+        ("gemm_ready_rowcol_16384x16384", lambda: synth.rowcol(),
+         lambda x, o: mxq.mx_quantize_rowcol(
+             x, mxq.ROWWISE | mxq.COLWISE | mxq.SCALE_RCEIL | mxq.SCALE_SWIZZLED, **o),
+         mx_bytes(16384, 16384), {}),
         ("dim1_colwise_16384x16384", lambda: synth.dim1(),
          lambda x, o: mxq.mx_quantize_rowcol(x, mxq.COLWISE, **o), mx_bytes(16384, 16384, rowwise=False),
          dict(q_col=None, s_col=None)),
