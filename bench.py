@@ -249,11 +249,25 @@ def time_device(fn, steps, warmup, world, stream):
     return total, per_call, max_over_ranks(total, world)
 
 
+# The pages' own cold-L2 kernel times for the same workload on GB200 (another
+# GPU: context for the cold figure beside them, not a target).  TE PR #3291
+# results tables: "specialized plain both 8192x28672", "generic dbias both
+# 8192x8192", "NVFP4 2D quantize-transpose both 8192x8192".
+PAGES_GB200_COLD_US = {
+    "rowcol_8192x28672": 149.4,
+    "dbias_rowcol_8192x8192": 52.5,
+    "nvfp4_2d_rowtrans_given_amax_8192x8192": 50.1,
+}
+
+
 def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None):
     """The other hot-path variants, each on its own workload (only the one
     named `only` when given)."""
     out = {}
     cases = [
+        ("rowcol_8192x28672", lambda: synth.rowcol(M=8192, K=28672),
+         lambda x, o: mxq.mx_quantize_rowcol(x, mxq.ROWWISE | mxq.COLWISE, **o),
+         mx_bytes(8192, 28672), {}),
         ("gemm_ready_rowcol_16384x16384", lambda: synth.rowcol(),
          lambda x, o: mxq.mx_quantize_rowcol(
              x, mxq.ROWWISE | mxq.COLWISE | mxq.SCALE_RCEIL | mxq.SCALE_SWIZZLED, **o),
@@ -332,6 +346,10 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
         if name.startswith("nvfp4_rowtrans_16"):
             out[name]["note"] = ("bytes exclude the tensor-amax pass (a second 256 MiB read), "
                                  "time includes it")
+        if name in PAGES_GB200_COLD_US:
+            cold_ms = cold_l2_measure(lambda: call(x, keep), 20, stream, device)
+            out[name]["cold_us_per_call"] = round(cold_ms * 1e3, 2)
+            out[name]["pages_gb200_cold_us"] = PAGES_GB200_COLD_US[name]
         if "given_amax" in name:
             out[name]["note"] = "tensor amax supplied by the caller: the quantize kernel alone"
             if name == "nvfp4_rowtrans_given_amax_16384x8192":

@@ -188,23 +188,23 @@ __device__ __forceinline__ uint32_t half16(uint32_t pair, int which) {
   return (pair >> (16 * which)) & 0xFFFFu;
 }
 
-// Exponent fields of a packed pair of bf16 magnitudes, as two 16-bit lanes.
-__device__ __forceinline__ uint32_t bf16_exponents(uint32_t m) { return (m >> 7) & 0x00FF00FFu; }
-
-// Scale exponents of a packed pair of bf16 magnitudes under the selected
-// rule: the exponent field (floor rule), plus one where the significand is
-// above 1.75 when ceil_mask is all ones (ceil rule: 2^(E-127) * m > 448 *
-// 2^(E-135) exactly when m > 1.75, so E - 8 + [m > 1.75] is
-// ceil(log2(amax / 448)) + 127).  The code is monotone in the amax, so
-// block maxima may be combined on these values.
-__device__ __forceinline__ uint32_t bf16_scale_exponents(uint32_t m, uint32_t ceil_mask) {
-  const uint32_t bump = (((m & 0x7Fu) > 0x60u) ? 1u : 0u) | ((((m >> 16) & 0x7Fu) > 0x60u) ? 0x10000u : 0u);
-  return bf16_exponents(m) + (bump & ceil_mask);
+// Scale exponents of a packed pair of bf16 maxima (two 16-bit lanes; the
+// sign bits carry no meaning) under the selected rule.  Floor rule
+// (ceil_add = 0): the exponent field E.  Ceil rule (ceil_add = 0x001F001F):
+// E + 1 where the significand is above 1.75, i.e. where the 7 stored
+// mantissa bits exceed 0x60 -- adding 0x1F to them carries into the
+// exponent field exactly then.  (2^(E-127) * m > 448 * 2^(E-135) exactly
+// when m > 1.75, so E - 8 + [m > 1.75] is ceil(log2(amax / 448)) + 127.)
+// For finite maxima the carry never leaves its lane.  The code is monotone
+// in the amax, so block maxima may be combined on these values.
+__device__ __forceinline__ uint32_t bf16_scale_exponents(uint32_t m, uint32_t ceil_add) {
+  return ((m + ceil_add) >> 7) & 0x00FF00FFu;
 }
 
-// The same for one fp32 magnitude (bits without the sign).
-__device__ __forceinline__ uint32_t f32_scale_exponent(uint32_t b, uint32_t ceil_mask) {
-  return (b >> 23) + (((b & 0x7FFFFFu) > 0x600000u ? 1u : 0u) & ceil_mask);
+// The same for one fp32 magnitude (bits without the sign); ceil_add is 0 or
+// 0x1FFFFF (23 mantissa bits above 0x600000 carry into the exponent).
+__device__ __forceinline__ uint32_t f32_scale_exponent(uint32_t b, uint32_t ceil_add) {
+  return (b + ceil_add) >> 23;
 }
 
 __device__ __forceinline__ void bar_sync_cta(int threads) {
@@ -361,7 +361,9 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   }
   __syncthreads();
 
-  const uint32_t ceil_mask = a.scale_ceil ? 0xFFFFFFFFu : 0u;   // scale rule
+  // Scale rule: the carry constants of bf16_scale_exponents / f32_scale_exponent.
+  const uint32_t ceil_bf16 = a.scale_ceil ? 0x001F001Fu : 0u;
+  const uint32_t ceil_f32 = a.scale_ceil ? 0x001FFFFFu : 0u;
   const int nmb = a.M / 32;    // colwise scale bytes per column
   const int nkb = a.K / 32;    // rowwise scale bytes per row
 
@@ -407,10 +409,10 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
             // low halves: even columns, high halves: odd columns; fold per row.
             re[i / 2] = bf16_scale_exponents(
-                absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)), ceil_mask);
+                absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)), ceil_bf16);
           }
 #pragma unroll
-          for (int p = 0; p < 4; ++p) ce[p] = bf16_scale_exponents(cm[p], ceil_mask);
+          for (int p = 0; p < 4; ++p) ce[p] = bf16_scale_exponents(cm[p], ceil_bf16);
         } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -448,12 +450,12 @@ mx_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            re[q] = f32_scale_exponent(rmx[2 * q], ceil_mask) |
-                    (f32_scale_exponent(rmx[2 * q + 1], ceil_mask) << 16);
+            re[q] = f32_scale_exponent(rmx[2 * q], ceil_f32) |
+                    (f32_scale_exponent(rmx[2 * q + 1], ceil_f32) << 16);
 #pragma unroll
           for (int p = 0; p < 4; ++p)
-            ce[p] = f32_scale_exponent(cmx[2 * p], ceil_mask) |
-                    (f32_scale_exponent(cmx[2 * p + 1], ceil_mask) << 16);
+            ce[p] = f32_scale_exponent(cmx[2 * p], ceil_f32) |
+                    (f32_scale_exponent(cmx[2 * p + 1], ceil_f32) << 16);
         }
       }
       // Column maxima over the warp's 16 rows, published for the partner warp
@@ -844,6 +846,9 @@ dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __r
 #ifndef MXQ_PLAIN_CPS
 #define MXQ_PLAIN_CPS 1
 #endif
+#ifndef MXQ_PLAIN_CPITCH
+#define MXQ_PLAIN_CPITCH 8
+#endif
 #ifndef MXQ_GELU_GROUP
 #define MXQ_GELU_GROUP 1
 #endif
@@ -933,7 +938,7 @@ cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
   // Column pitch of the colwise scale staging (four blocks per column).  The
   // pitch changes how the warps' store phases line up; measured on GB300,
   // 8 bytes is faster for the plain cast and 4 bytes for the fused paths.
-  constexpr int CPITCH = (ACT == ACT_NONE && !DBIAS) ? 8 : 4;
+  constexpr int CPITCH = (ACT == ACT_NONE && !DBIAS) ? MXQ_PLAIN_CPITCH : 4;
   // Rowwise codes: staged and sent by one bulk store per step, or streaming
   // stores straight from registers.  Measured on GB300 (A/B): the bulk store
   // is faster for GELU (108 -> 94 us), dbias (64.6 -> 63 us) and the

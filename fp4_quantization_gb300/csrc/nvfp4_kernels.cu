@@ -165,36 +165,10 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int c = lane & 7;    // 8-column chunk 0..7
   const uint32_t bar0 = smem_addr(&full_bar[0]);
 
-  const float A = *a.amax;
-  const float G = __fdiv_rn(A, 2688.0f);
-  if (blockIdx.x == 0 && tid == 0) *a.global_scale = G;
-
-  // Scale tables (see NvScaleTables).
-  NvScaleTables tabs;
-  tabs.G = G;
-  tabs.code_tab = sbase + NV_OFF_CODE;
-  tabs.inv_tab = sbase + NV_OFF_INV;
-  {
-    const int ea = static_cast<int>((__float_as_uint(A) >> 23) & 0xFFu);
-    const int lo_e = ea > NV_TAB_BINADES - 1 ? ea - (NV_TAB_BINADES - 1) : 0;
-    tabs.lo_bits = static_cast<uint32_t>(lo_e) << 7;
-    tabs.hi_bits = (static_cast<uint32_t>(ea) << 7) | 0x7Fu;
-    const int entries = static_cast<int>(tabs.hi_bits - tabs.lo_bits) + 1;
-    for (int e = tid; e < entries; e += NV_WARPS * 32) {
-      uint32_t code;
-      float inv;
-      nv_block_scale(__uint_as_float((tabs.lo_bits + e) << 16), G, code, inv);
-      sts8(tabs.code_tab + e, code);
-    }
-    for (int cd = tid; cd < 128; cd += NV_WARPS * 32)
-      sts32(tabs.inv_tab + 4 * cd, __float_as_uint(nv_inv_from_code(cd, G)));
-  }
-
   const int64_t total = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
   const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
   const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
   const int count = t1 - t0;
-  if (count <= 0) return;
 
   auto issue_load = [&](int j) {   // thread 0 only
     const int t = t0 + j;
@@ -219,6 +193,34 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     fence_barrier_init();
     for (int jj = 0; jj < NV_STAGES && jj < count; ++jj) issue_load(jj);
   }
+
+  // The tensor amax, read while the first copies are in flight.
+  const float A = *a.amax;
+  const float G = __fdiv_rn(A, 2688.0f);
+  if (blockIdx.x == 0 && tid == 0) *a.global_scale = G;
+  if (count <= 0) return;
+
+  // Scale tables (see NvScaleTables).
+  NvScaleTables tabs;
+  tabs.G = G;
+  tabs.code_tab = sbase + NV_OFF_CODE;
+  tabs.inv_tab = sbase + NV_OFF_INV;
+  {
+    const int ea = static_cast<int>((__float_as_uint(A) >> 23) & 0xFFu);
+    const int lo_e = ea > NV_TAB_BINADES - 1 ? ea - (NV_TAB_BINADES - 1) : 0;
+    tabs.lo_bits = static_cast<uint32_t>(lo_e) << 7;
+    tabs.hi_bits = (static_cast<uint32_t>(ea) << 7) | 0x7Fu;
+    const int entries = static_cast<int>(tabs.hi_bits - tabs.lo_bits) + 1;
+    for (int e = tid; e < entries; e += NV_WARPS * 32) {
+      uint32_t code;
+      float inv;
+      nv_block_scale(__uint_as_float((tabs.lo_bits + e) << 16), G, code, inv);
+      sts8(tabs.code_tab + e, code);
+    }
+    for (int cd = tid; cd < 128; cd += NV_WARPS * 32)
+      sts32(tabs.inv_tab + 4 * cd, __float_as_uint(nv_inv_from_code(cd, G)));
+  }
+
   __syncthreads();
 
   const int nkb = a.K / 16;   // rowwise scale bytes per row
