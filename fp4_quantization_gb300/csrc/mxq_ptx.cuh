@@ -83,6 +83,23 @@ __device__ __forceinline__ void stg32(void* p, uint32_t a) {
   asm volatile("st.global.b32 [%0], %1;" :: "l"(p), "r"(a) : "memory");
 }
 
+// 16- and 8-byte stores with an L2 cache policy for the written line.
+__device__ __forceinline__ void stg128_hint(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+               :: "l"(p), "r"(a), "r"(b), "r"(c), "r"(d), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ void stg64_hint(void* p, uint32_t a, uint32_t b, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;"
+               :: "l"(p), "r"(a), "r"(b), "l"(policy) : "memory");
+}
+
+// 4-byte store with an L2 cache policy for the written line.
+__device__ __forceinline__ void stg32_hint(void* p, uint32_t a, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" :: "l"(p), "r"(a), "l"(policy) : "memory");
+}
+
 __device__ __forceinline__ void stg8(void* p, uint32_t a) {
   asm volatile("st.global.u8 [%0], %1;" :: "l"(p), "r"(a) : "memory");
 }
@@ -187,6 +204,27 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_store_3d with an L2 cache policy for the written lines.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, uint32_t src, int x,
+                                                  int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;"
+      :: "l"(map), "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy) : "memory");
 }
 
 // tma_load_2d with an L2 cache policy for the loaded lines.

@@ -223,6 +223,7 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
   __syncthreads();
 
+  const uint64_t tsc_policy = l2_policy_evict_last();
   const int nkb = a.K / 16;   // rowwise scale bytes per row
   const int nmb = a.M / 16;   // transposed scale bytes per column
   int rq_first = -1;          // first slot of the rowwise code group gathered
@@ -425,7 +426,9 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
           const uint32_t wv[4] = {pick4(rot, r), pick4(rot, (r + 1) & 3), pick4(rot, (r + 2) & 3),
                                   pick4(rot, (r + 3) & 3)};
           if (nvalid == 16 && (nmb & 15) == 0) {
-            stg128(dst, wv[0], wv[1], wv[2], wv[3]);
+            // Half of a 32-byte sector whose other half another CTA writes:
+            // evict-last keeps it in L2 until the sector is whole.
+            stg128_hint(dst, wv[0], wv[1], wv[2], wv[3], tsc_policy);
           } else {
             for (int bb = 0; bb < nvalid; ++bb) stg8(dst + bb, (wv[bb >> 2] >> (8 * (bb & 3))) & 0xFFu);
           }
