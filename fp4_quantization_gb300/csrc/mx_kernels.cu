@@ -322,6 +322,10 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
   // inside a group the steps run column by column, the group's bands
   // interleaved, so the colwise output of GROUP consecutive bands (and their
   // colwise scale bytes) is written by one CTA in consecutive steps.
+  // dbias: the finalize grid (launched as a programmatic dependent) may be
+  // scheduled now; it waits for this grid's completion before reading.
+  if constexpr (DBIAS) grid_launch_dependents();
+
   const int64_t total = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
   const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
   const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
@@ -853,6 +857,7 @@ constexpr int kFinalizeCols = 64;
 __global__ void __launch_bounds__(4 * kFinalizeCols)
 dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __restrict__ dbias) {
   __shared__ float part[4][kFinalizeCols];
+  grid_dependency_wait();   // the band sums of the quantize grid before it
   const int kc = threadIdx.x % kFinalizeCols, q = threadIdx.x / kFinalizeCols;
   const int k = blockIdx.x * kFinalizeCols + kc;
   const int per = (bands + 3) / 4;
@@ -1066,9 +1071,19 @@ int mx_band_rows(int act) {
 
 cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
                                   cudaStream_t stream) {
-  const int blocks = (K + kFinalizeCols - 1) / kFinalizeCols;
-  dbias_finalize_kernel<<<blocks, 4 * kFinalizeCols, 0, stream>>>(ws, bands, K, dbias);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the quantize grid just before it
+  // on the stream, so its launch overlaps that grid's last steps.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((K + kFinalizeCols - 1) / kFinalizeCols);
+  cfg.blockDim = dim3(4 * kFinalizeCols);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dbias_finalize_kernel, ws, bands, K, dbias);
 }
 
 #endif

@@ -526,7 +526,7 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t);
   if (st != MXQ_OK) return st;
   return from_cuda(mxq::launch_nvfp4(maps, a, direction_mode(flags), (flags & MXQ_NVFP4_2D) != 0,
-                                     sms, stream));
+                                     sms, amax_in == nullptr, stream));
 }
 
 mxq_status mxq_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* dev_err, mxq_stream_t stream) {

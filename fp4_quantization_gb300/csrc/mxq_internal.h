@@ -96,8 +96,10 @@ cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbia
                                   cudaStream_t stream);
 int nv_band_rows();
 int nv_step_cols();
+// after_amax: launched right after this call's own bf16_amax grid (as its
+// programmatic dependent).
 cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two_d,
-                         int num_sms, cudaStream_t stream);
+                         int num_sms, bool after_amax, cudaStream_t stream);
 cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,
                              int num_sms, cudaStream_t stream);
 cudaError_t launch_nv_global_scale(const float* amax, float* global_scale, cudaStream_t stream);

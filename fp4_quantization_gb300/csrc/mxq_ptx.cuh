@@ -83,6 +83,18 @@ __device__ __forceinline__ void stg32(void* p, uint32_t a) {
   asm volatile("st.global.b32 [%0], %1;" :: "l"(p), "r"(a) : "memory");
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start once every CTA of the grid before it has signalled
+// launch_dependents (or exited); grid_dependency_wait then blocks until that
+// grid has completed and its writes are visible.  Without a programmatic
+// dependency the wait returns at once.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // 16- and 8-byte stores with an L2 cache policy for the written line.
 __device__ __forceinline__ void stg128_hint(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
                                             uint64_t policy) {

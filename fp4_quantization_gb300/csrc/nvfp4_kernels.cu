@@ -194,7 +194,9 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     for (int jj = 0; jj < NV_STAGES && jj < count; ++jj) issue_load(jj);
   }
 
-  // The tensor amax, read while the first copies are in flight.
+  // The tensor amax, read while the first copies are in flight (after the
+  // amax grid this one may depend on has completed).
+  grid_dependency_wait();
   const float A = *a.amax;
   const float G = __fdiv_rn(A, 2688.0f);
   if (blockIdx.x == 0 && tid == 0) *a.global_scale = G;
@@ -501,6 +503,9 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 __global__ void __launch_bounds__(256)
 bf16_amax_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                  unsigned int* __restrict__ out) {
+  // A quantize grid launched as a programmatic dependent may be scheduled
+  // now: it reads only the input until it has waited for this grid.
+  grid_launch_dependents();
   const int64_t chunks = K / 8;
   uint32_t m = 0u;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
@@ -543,7 +548,7 @@ __global__ void selftest_wait_kernel(uint64_t timeout_ns, uint32_t* dev_err) {
 }
 
 template <int MODE, bool TWO_D>
-cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms,
+cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms, bool after_amax,
                               cudaStream_t stream) {
   auto kernel = nvfp4_quantize_kernel<MODE, TWO_D>;
   static int configured_device = -1;
@@ -557,17 +562,31 @@ cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms,
   }
   const int64_t steps = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
   const int grid = static_cast<int>(steps < num_sms ? steps : num_sms);
-  kernel<<<grid < 1 ? 1 : grid, NV_WARPS * 32, NV_SMEM, stream>>>(maps.x, maps.q_row, maps.q_t, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid < 1 ? 1 : grid);
+  cfg.blockDim = dim3(NV_WARPS * 32);
+  cfg.dynamicSmemBytes = NV_SMEM;
+  cfg.stream = stream;
+  // Right after this call's own amax grid, launched as its programmatic
+  // dependent: the first input copies and the set-up overlap the amax
+  // grid's tail (the kernel waits for it before reading the amax).  Never
+  // after a caller's kernel, which may still be writing the input.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_amax ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, maps.x, maps.q_row, maps.q_t, a);
 }
 
 template <bool TWO_D>
 cudaError_t launch_nv_mode(const NvMaps& maps, const NvArgs& a, int mode, int num_sms,
-                           cudaStream_t stream) {
+                           bool after_amax, cudaStream_t stream) {
   switch (mode) {
-    case MX_ROW: return launch_nv_variant<MX_ROW, TWO_D>(maps, a, num_sms, stream);
-    case MX_COL: return launch_nv_variant<MX_COL, TWO_D>(maps, a, num_sms, stream);
-    default: return launch_nv_variant<MX_ROW | MX_COL, TWO_D>(maps, a, num_sms, stream);
+    case MX_ROW: return launch_nv_variant<MX_ROW, TWO_D>(maps, a, num_sms, after_amax, stream);
+    case MX_COL: return launch_nv_variant<MX_COL, TWO_D>(maps, a, num_sms, after_amax, stream);
+    default:
+      return launch_nv_variant<MX_ROW | MX_COL, TWO_D>(maps, a, num_sms, after_amax, stream);
   }
 }
 
@@ -577,9 +596,9 @@ int nv_band_rows() { return NV_BAND; }
 int nv_step_cols() { return NV_STEP_K; }
 
 cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two_d,
-                         int num_sms, cudaStream_t stream) {
-  return two_d ? launch_nv_mode<true>(maps, a, mode, num_sms, stream)
-               : launch_nv_mode<false>(maps, a, mode, num_sms, stream);
+                         int num_sms, bool after_amax, cudaStream_t stream) {
+  return two_d ? launch_nv_mode<true>(maps, a, mode, num_sms, after_amax, stream)
+               : launch_nv_mode<false>(maps, a, mode, num_sms, after_amax, stream);
 }
 
 cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,
