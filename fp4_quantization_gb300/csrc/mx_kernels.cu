@@ -68,7 +68,7 @@
 // 3 evict-normal; rowwise code stores streaming (.cs) or plain.  Copies two
 // ring slots at a time when MXQ_LOAD_PAIR (even slot counts).
 #ifndef MXQ_LOAD_POLICY
-#define MXQ_LOAD_POLICY 2
+#define MXQ_LOAD_POLICY 3
 #endif
 #ifndef MXQ_QCOL_POLICY
 #define MXQ_QCOL_POLICY 0
@@ -357,12 +357,14 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
     p0.bi = local - p0.tk * p0.nb;
   }
   Pos lpos = p0;   // next step to load (thread 0)
-  // The input tiles are loaded with the evict-last L2 policy and the rowwise
-  // codes stored with the streaming (.cs) operator, so that L2 gives up the
-  // written lines first and writes them back while the reads stream in.
-  // Measured on GB300 (16384x16384 rowwise+colwise): 203 -> 195 us; the
-  // input's lines keep their high priority in L2 after the call.
-  // L2 policy of the colwise scale runs (row-major scales).
+  // L2 policies.  Rowwise codes leave with the streaming (.cs) operator, so
+  // L2 gives their lines up first and writes them back while the reads
+  // stream in; the colwise scale runs (row-major scales: an eighth of a
+  // sector each, completed by other CTAs later) are kept with evict-last
+  // until their sectors are whole; the input tiles are loaded evict-normal,
+  // below the scale runs.  Measured on GB300 against evict-last input tiles:
+  // 16384^2 184.5 -> 180.4 us, 8192x28672 173.0 -> 159.7 us, 16384x28672
+  // 363.4 -> 317.8 us (the wider the matrix, the more scale runs wait in L2).
   const uint64_t csc_policy = MXQ_CSC_POLICY == 3 ? l2_policy_evict_normal() : l2_policy_evict_last();
 #if MXQ_LOAD_POLICY == 1
   const uint64_t load_policy = l2_policy_evict_first();

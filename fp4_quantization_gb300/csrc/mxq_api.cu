@@ -521,12 +521,13 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   mxq::NvMaps maps{};
+  const int mode = direction_mode(flags);
+  const bool two_d = (flags & MXQ_NVFP4_2D) != 0;
   st = encode_bf16_map(&maps.x, x, M, K, ldx, step, band);
   if (st != MXQ_OK) return st;
   st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t);
   if (st != MXQ_OK) return st;
-  return from_cuda(mxq::launch_nvfp4(maps, a, direction_mode(flags), (flags & MXQ_NVFP4_2D) != 0,
-                                     sms, amax_in == nullptr, stream));
+  return from_cuda(mxq::launch_nvfp4(maps, a, mode, two_d, sms, amax_in == nullptr, stream));
 }
 
 mxq_status mxq_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* dev_err, mxq_stream_t stream) {

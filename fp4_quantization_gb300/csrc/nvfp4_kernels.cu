@@ -67,10 +67,11 @@ constexpr int NV_OFF_RSC = NV_OFF_QR + NV_BAND * 128;
 // column k are rotated by (k / 8) % 4 so that the lanes storing the columns
 // 8 apart use different banks.
 constexpr int NV_OFF_TSC = NV_OFF_RSC + NV_BAND * NV_RSC_PITCH;
-constexpr int NV_OFF_INV = NV_OFF_TSC + NV_STEP_K * 16;          // [128] fp32 1/d per code
-constexpr int NV_TAB_BINADES = 21;                               // code table: binades kept
-constexpr int NV_OFF_CODE = NV_OFF_INV + 128 * 4;                // [21 x 128] E4M3 codes
-constexpr int NV_SMEM = NV_OFF_CODE + NV_TAB_BINADES * 128 + 1024;   // + alignment pad
+constexpr int NV_TAB_BINADES = 21;                               // scale table: binades kept
+// Scale table: [21 x 128 + 2] entries of {fp32 1/d, code} (see NvScaleTables).
+constexpr int NV_OFF_TAB = NV_OFF_TSC + NV_STEP_K * 16;
+constexpr int NV_TAB_ENTRIES = NV_TAB_BINADES * 128 + 2;
+constexpr int NV_SMEM = NV_OFF_TAB + NV_TAB_ENTRIES * 8 + 1024;   // + alignment pad
 
 __device__ __forceinline__ void bar_sync_nv() {
   asm volatile("bar.sync 1, %0;" :: "r"(NV_WARPS * 32) : "memory");
@@ -92,41 +93,55 @@ __device__ __forceinline__ void nv_block_scale(float b, float G, uint32_t& code,
 
 // One bf16 magnitude of a packed pair of maxima, as its 15 magnitude bits
 // (the sign bit left by max.xorsign.abs carries no meaning and is dropped).
-// 1 / (value(code) * G) as nv_block_scale computes it (0 for code 0 or a
-// zero product, the largest finite float if the reciprocal overflows).
-__device__ __forceinline__ float nv_inv_from_code(uint32_t code, float G) {
-  const float d = __fmul_rn(e4m3_to_f32(code), G);
-  if (code == 0u || d == 0.0f) return 0.0f;
-  const float inv = __frcp_rn(d);
-  return isinf(inv) ? FLT_MAX : inv;
-}
-
 __device__ __forceinline__ uint32_t mag16(uint32_t pair, int which) {
   return (pair >> (16 * which)) & 0x7FFFu;
 }
 
 // Scale code of a block and the reciprocal its elements are multiplied by.
-// With G fixed for the tensor, the code depends only on the block amax b and
-// 1/d only on the code, so both come from per-CTA tables filled with the
-// exact arithmetic of nv_block_scale: codes for the NV_TAB_BINADES binades
-// of bf16 magnitudes at and below the tensor amax (anything smaller gives
-// b / (6 G) below 2^-10, i.e. code 0), reciprocals for the 127 positive
-// codes.  A block amax above the table (possible only when the caller's
-// amax is smaller than the data) takes the direct computation.
+// With G fixed for the tensor, both depend only on the block amax b, so they
+// come from one per-CTA table filled with the exact arithmetic of
+// nv_block_scale, one 8-byte entry {1/d, code} per bf16 magnitude of the
+// NV_TAB_BINADES binades at and below the tensor amax, plus one entry on
+// each side:
+//  * below: anything smaller gives b / (6 G) below 2^-10, i.e. code 0;
+//  * above (a block amax beyond the tensor amax's binade, possible only when
+//    the caller's amax is smaller than the data): b > A, so b / (6 G) rounds
+//    to at least 448 and saturates to code 0x7E (0 when G is 0), the result
+//    of nv_block_scale for the first magnitude above the table; the code is
+//    monotone in b and 1/d depends only on the code.
+// The lookup is a clamp and one 8-byte shared load, without a branch.
 struct NvScaleTables {
-  uint32_t code_tab, inv_tab;   // shared addresses
-  uint32_t lo_bits, hi_bits;    // magnitude bits covered: [lo_bits, hi_bits]
-  float G;
+  uint32_t tab;    // shared address of entry 0 (the "below" entry)
+  int base;        // magnitude bits of entry 1, minus 1
+  int top;         // index of the "above" entry
 
   __device__ __forceinline__ void lookup(uint32_t mag, uint32_t& code, float& inv) const {
-    if (mag > hi_bits) {
-      nv_block_scale(__uint_as_float(mag << 16), G, code, inv);
-      return;
-    }
-    code = mag >= lo_bits ? ld_shared_u8(code_tab + (mag - lo_bits)) : 0u;
-    inv = __uint_as_float(lds32(inv_tab + 4 * code));
+    const int idx = min(max(static_cast<int>(mag) - base, 0), top);
+    const uint2 e = lds64(tab + 8 * idx);
+    inv = __uint_as_float(e.x);
+    code = e.y;
   }
 };
+
+// Fills this CTA's scale table (see NvScaleTables) for tensor amax A and
+// G = A / 2688; the caller synchronises the CTA before the first lookup.
+__device__ __forceinline__ NvScaleTables nv_build_tables(uint32_t sbase, float A, float G, int tid) {
+  NvScaleTables tabs;
+  tabs.tab = sbase + NV_OFF_TAB;
+  const int ea = static_cast<int>((__float_as_uint(A) >> 23) & 0xFFu);
+  const int lo_e = ea > NV_TAB_BINADES - 1 ? ea - (NV_TAB_BINADES - 1) : 0;
+  const int lo_bits = lo_e << 7;
+  const int hi_bits = (ea << 7) | 0x7F;
+  tabs.base = lo_bits - 1;
+  tabs.top = hi_bits - lo_bits + 2;
+  for (int e = tid; e <= tabs.top; e += NV_WARPS * 32) {
+    uint32_t code = 0u;
+    float inv = 0.0f;
+    if (e > 0) nv_block_scale(__uint_as_float(static_cast<uint32_t>(tabs.base + e) << 16), G, code, inv);
+    sts64(tabs.tab + 8 * e, __float_as_uint(inv), code);
+  }
+  return tabs;
+}
 
 // Swizzled byte offset inside a [rows][128 B] staging block whose TMA map
 // uses the 128-byte swizzle: the 16-byte chunk index is xor-ed with the
@@ -142,6 +157,61 @@ __device__ __forceinline__ uint32_t tsc_offset(int col, int blk) {
 
 __device__ __forceinline__ uint32_t pick4(const uint32_t v[4], int i) {
   return (i & 2) ? ((i & 1) ? v[3] : v[2]) : ((i & 1) ? v[1] : v[0]);
+}
+
+// Transposed scale bytes of one step (staged as [64 columns][16 blocks],
+// word j of column k rotated to (j + k / 8) % 4): 16 bytes per column; warp w
+// writes columns 8w .. 8w + 7.  A run is half of a 32-byte sector whose other
+// half the CTA of the next band writes: evict-last keeps it in L2 until the
+// sector is whole.
+__device__ __forceinline__ void nv_flush_tscales(const NvArgs& a, uint32_t sbase, int band, int tk,
+                                                 int warp, int lane, uint64_t tsc_policy) {
+  const int nmb = a.M / 16;
+  if (lane < NV_STEP_K / NV_WARPS) {
+    const int kc = warp * (NV_STEP_K / NV_WARPS) + lane;
+    const int k = tk * NV_STEP_K + kc;
+    const int mb0 = band * (NV_BAND / 16);
+    const int nvalid = min(NV_BAND / 16, nmb - mb0);
+    if (k < a.K) {
+      uint8_t* dst = a.s_t + static_cast<size_t>(k) * nmb + mb0;
+      const uint4 v = lds128(sbase + NV_OFF_TSC + kc * 16);
+      const uint32_t rot[4] = {v.x, v.y, v.z, v.w};
+      const int r = (kc >> 3) & 3;   // word j of the column is stored at (j + r) % 4
+      const uint32_t wv[4] = {pick4(rot, r), pick4(rot, (r + 1) & 3), pick4(rot, (r + 2) & 3),
+                              pick4(rot, (r + 3) & 3)};
+      if (nvalid == 16 && (nmb & 15) == 0) {
+        stg128_hint(dst, wv[0], wv[1], wv[2], wv[3], tsc_policy);
+      } else {
+        for (int bb = 0; bb < nvalid; ++bb) stg8(dst + bb, (wv[bb >> 2] >> (8 * (bb & 3))) & 0xFFu);
+      }
+    }
+  }
+}
+
+// Rowwise scale bytes of steps first..slot8 of a group of eight (staged as
+// [256 rows][36-byte pitch], 4 bytes per step): eight steps are one 32-byte
+// sector per row, written by two neighbouring threads in one instruction (16
+// bytes each) so the sector leaves as one request.
+__device__ __forceinline__ void nv_flush_rscales(const NvArgs& a, uint32_t sbase, int band, int tk,
+                                                 int first, int slot8, int tid) {
+  const int nkb = a.K / 16;
+  const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
+  // Two 16-byte halves: every row start must be 16-byte aligned.
+  const bool full = first == 0 && slot8 == 7 && (nkb & 15) == 0;
+  for (int it = tid; it < 2 * NV_BAND; it += NV_WARPS * 32) {
+    const int rr = it >> 1, half = it & 1;
+    const int row = band * NV_BAND + rr;
+    if (row >= a.M) continue;
+    uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
+    const uint32_t src = sbase + NV_OFF_RSC + rr * NV_RSC_PITCH;
+    if (full) {
+      const uint32_t s16 = src + 16 * half;
+      stg128(dst + 16 * half, lds32(s16), lds32(s16 + 4), lds32(s16 + 8), lds32(s16 + 12));
+    } else if (half == 0) {
+      const int b_end = min((slot8 + 1) * 4, nkb - kb0);
+      copy_run_to_global(dst + first * 4, src + first * 4, b_end - first * 4);
+    }
+  }
 }
 
 template <int MODE, bool TWO_D>
@@ -203,31 +273,10 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   if (count <= 0) return;
 
   // Scale tables (see NvScaleTables).
-  NvScaleTables tabs;
-  tabs.G = G;
-  tabs.code_tab = sbase + NV_OFF_CODE;
-  tabs.inv_tab = sbase + NV_OFF_INV;
-  {
-    const int ea = static_cast<int>((__float_as_uint(A) >> 23) & 0xFFu);
-    const int lo_e = ea > NV_TAB_BINADES - 1 ? ea - (NV_TAB_BINADES - 1) : 0;
-    tabs.lo_bits = static_cast<uint32_t>(lo_e) << 7;
-    tabs.hi_bits = (static_cast<uint32_t>(ea) << 7) | 0x7Fu;
-    const int entries = static_cast<int>(tabs.hi_bits - tabs.lo_bits) + 1;
-    for (int e = tid; e < entries; e += NV_WARPS * 32) {
-      uint32_t code;
-      float inv;
-      nv_block_scale(__uint_as_float((tabs.lo_bits + e) << 16), G, code, inv);
-      sts8(tabs.code_tab + e, code);
-    }
-    for (int cd = tid; cd < 128; cd += NV_WARPS * 32)
-      sts32(tabs.inv_tab + 4 * cd, __float_as_uint(nv_inv_from_code(cd, G)));
-  }
-
+  const NvScaleTables tabs = nv_build_tables(sbase, A, G, tid);
   __syncthreads();
 
   const uint64_t tsc_policy = l2_policy_evict_last();
-  const int nkb = a.K / 16;   // rowwise scale bytes per row
-  const int nmb = a.M / 16;   // transposed scale bytes per column
   int rq_first = -1;          // first slot of the rowwise code group gathered
   int rs_first = -1;          // first slot of the rowwise scale group gathered
 
@@ -414,28 +463,7 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         tma_store_3d(&tmap_qt, sbase + NV_OFF_QT, band * (NV_BAND / 2), tk * (NV_STEP_K / 8), 0);
         bulk_commit();
       }
-      // Transposed scale bytes: 16 per column per step; warp w takes 8 columns.
-      if (lane < NV_STEP_K / NV_WARPS) {
-        const int kc = warp * (NV_STEP_K / NV_WARPS) + lane;
-        const int k = tk * NV_STEP_K + kc;
-        const int mb0 = band * (NV_BAND / 16);
-        const int nvalid = min(NV_BAND / 16, nmb - mb0);
-        if (k < a.K) {
-          uint8_t* dst = a.s_t + static_cast<size_t>(k) * nmb + mb0;
-          const uint4 v = lds128(sbase + NV_OFF_TSC + kc * 16);
-          const uint32_t rot[4] = {v.x, v.y, v.z, v.w};
-          const int r = (kc >> 3) & 3;   // word j of the column is stored at (j + r) % 4
-          const uint32_t wv[4] = {pick4(rot, r), pick4(rot, (r + 1) & 3), pick4(rot, (r + 2) & 3),
-                                  pick4(rot, (r + 3) & 3)};
-          if (nvalid == 16 && (nmb & 15) == 0) {
-            // Half of a 32-byte sector whose other half another CTA writes:
-            // evict-last keeps it in L2 until the sector is whole.
-            stg128_hint(dst, wv[0], wv[1], wv[2], wv[3], tsc_policy);
-          } else {
-            for (int bb = 0; bb < nvalid; ++bb) stg8(dst + bb, (wv[bb >> 2] >> (8 * (bb & 3))) & 0xFFu);
-          }
-        }
-      }
+      nv_flush_tscales(a, sbase, band, tk, warp, lane, tsc_policy);
     }
 
     if constexpr (ROW) {
@@ -466,29 +494,11 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
         rq_first = -1;
       }
-      // Rowwise scale bytes: eight steps = one 32-byte sector per row, written
-      // by two neighbouring threads in one instruction (16 bytes each) so the
-      // sector leaves as one request.
+      // Rowwise scale bytes, once per group of eight steps.
       const int slot8 = tk & 7;
       if (rs_first < 0) rs_first = slot8;
       if (slot8 == 7 || end) {
-        const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
-        // Two 16-byte halves: every row start must be 16-byte aligned.
-        const bool full = rs_first == 0 && slot8 == 7 && (nkb & 15) == 0;
-        for (int it = tid; it < 2 * NV_BAND; it += NV_WARPS * 32) {
-          const int rr = it >> 1, half = it & 1;
-          const int row = band * NV_BAND + rr;
-          if (row >= a.M) continue;
-          uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
-          const uint32_t src = sbase + NV_OFF_RSC + rr * NV_RSC_PITCH;
-          if (full) {
-            const uint32_t s16 = src + 16 * half;
-            stg128(dst + 16 * half, lds32(s16), lds32(s16 + 4), lds32(s16 + 8), lds32(s16 + 12));
-          } else if (half == 0) {
-            const int b_end = min((slot8 + 1) * 4, nkb - kb0);
-            copy_run_to_global(dst + rs_first * 4, src + rs_first * 4, b_end - rs_first * 4);
-          }
-        }
+        nv_flush_rscales(a, sbase, band, tk, rs_first, slot8, tid);
         rs_first = -1;
       }
     }
@@ -547,11 +557,15 @@ __global__ void selftest_wait_kernel(uint64_t timeout_ns, uint32_t* dev_err) {
   if (__any_sync(0xFFFFFFFFu, !ok) && threadIdx.x == 0) atomicOr(dev_err, 1u);
 }
 
-template <int MODE, bool TWO_D>
-cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms, bool after_amax,
-                              cudaStream_t stream) {
-  auto kernel = nvfp4_quantize_kernel<MODE, TWO_D>;
-  static int configured_device = -1;
+using NvKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, NvArgs);
+
+// One launch of an NVFP4 kernel: one persistent CTA per SM (or per step).
+// Right after this call's own amax grid it is launched as that grid's
+// programmatic dependent: the first input copies and the set-up overlap the
+// amax grid's tail (the kernel waits for it before reading the amax).  Never
+// after a caller's kernel, which may still be writing the input.
+cudaError_t launch_nv_kernel(NvKernel kernel, int& configured_device, const NvMaps& maps,
+                             const NvArgs& a, int num_sms, bool after_amax, cudaStream_t stream) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -567,16 +581,20 @@ cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms, 
   cfg.blockDim = dim3(NV_WARPS * 32);
   cfg.dynamicSmemBytes = NV_SMEM;
   cfg.stream = stream;
-  // Right after this call's own amax grid, launched as its programmatic
-  // dependent: the first input copies and the set-up overlap the amax
-  // grid's tail (the kernel waits for it before reading the amax).  Never
-  // after a caller's kernel, which may still be writing the input.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_amax ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, maps.x, maps.q_row, maps.q_t, a);
+}
+
+template <int MODE, bool TWO_D>
+cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms, bool after_amax,
+                              cudaStream_t stream) {
+  static int configured_device = -1;
+  return launch_nv_kernel(nvfp4_quantize_kernel<MODE, TWO_D>, configured_device, maps, a, num_sms,
+                          after_amax, stream);
 }
 
 template <bool TWO_D>

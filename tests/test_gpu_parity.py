@@ -352,8 +352,8 @@ def test_nvfp4_given_amax_and_hand_block():
 
 @pytest.mark.parametrize("amax_factor", [0.25, 1.0, 3.0])
 def test_nvfp4_caller_amax(amax_factor):
-    """A caller amax below the data's (block amaxes above it take the direct
-    scale computation), equal to it, and above it."""
+    """A caller amax below the data's (block amaxes beyond its binade take the
+    saturated scale, code 0x7E), equal to it, and above it."""
     bits = synth.nvfp4(M=256, K=512, seed=51)
     A = np.float32(oracle.bf16_amax(bits) * amax_factor)
     x = to_device(bits)
