@@ -81,6 +81,10 @@
 #endif
 // L2 policy of the colwise scale runs (row-major scales): 2 evict-last,
 // 3 evict-normal.
+// Rowwise codes of the plain cast by bulk tensor store (tuning builds).
+#ifndef MXQ_PLAIN_RTMA
+#define MXQ_PLAIN_RTMA 0
+#endif
 #ifndef MXQ_CSC_POLICY
 #define MXQ_CSC_POLICY 2
 #endif
@@ -743,7 +747,7 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
                              (static_cast<size_t>(ktile) * tiles_m + pos.g * GROUP + bb) * 512 + 16 * ln;
               stg128(dst, w[0], w[1], w[2], w[3]);
             }
-          } else if (nblk == NB && (nmb % CH) == 0) {
+          } else if (nblk == NB && (nmb % CH) == 0 && (a.scol_ld % CH) == 0) {
             // Item i = (chunk, column); warp w takes items w * IPW .. + IPW - 1.
             constexpr int ITEMS = MX_TILE_K * (NB / CH);
             constexpr int IPW = ITEMS / WARPS;
@@ -761,7 +765,7 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
                   w[bb >> 2] |= ld_shared_u8(sbase + L::OFF_CSC + L::csc(ch * CH + bb, kc))
                                 << (8 * (bb & 3));
               }
-              uint8_t* dst = a.s_col + static_cast<size_t>(obase + k) * nmb + mb0 + ch * CH;
+              uint8_t* dst = a.s_col + static_cast<size_t>(obase + k) * a.scol_ld + mb0 + ch * CH;
               if (k < a.kin) {
                 // Evict-last: a run is part of a 32-byte sector that other
                 // CTAs complete later; kept in L2 until then, the sector is
@@ -776,7 +780,7 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
             for (int kc = tid; kc < MX_TILE_K; kc += THREADS) {
               const int k = tk * MX_TILE_K + kc;
               if (k >= a.kin) continue;
-              uint8_t* dst = a.s_col + static_cast<size_t>(obase + k) * nmb + mb0;
+              uint8_t* dst = a.s_col + static_cast<size_t>(obase + k) * a.scol_ld + mb0;
               for (int bb = 0; bb < nblk; ++bb)
                 stg8(dst + bb, ld_shared_u8(sbase + L::OFF_CSC + L::csc(fb * L::BPB + bb, kc)));
             }
@@ -1017,7 +1021,8 @@ cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
   // is faster for GELU (108 -> 94 us), dbias (64.6 -> 63 us) and the
   // single-input backward (dbias_dgelu 164 -> 157 us), slower for the plain
   // cast (196 -> 210 us) and the gated forward (121 -> 123 us).
-  constexpr bool RTMA = ACT == ACT_GELU || DBIAS || ACT == ACT_DGELU || ACT == ACT_DSILU;
+  constexpr bool RTMA = ACT == ACT_GELU || DBIAS || ACT == ACT_DGELU || ACT == ACT_DSILU ||
+                        (MXQ_PLAIN_RTMA && ACT == ACT_NONE);
   using L = MxLayout<WARPS, act_operands(ACT), STAGES, GROUP, QBUF, CPITCH, act_outputs(ACT),
                      RTMA>;
   static_assert(L::DYNAMIC <= 227 * 1024, "shared memory per CTA");

@@ -159,35 +159,13 @@ int direction_mode(uint32_t flags) {
 
 }  // namespace
 
-extern "C" {
+namespace mxq {
 
-const char* mxq_status_string(int status) {
-  switch (status) {
-    case MXQ_OK: return "MXQ_OK";
-    case MXQ_EINVAL: return "MXQ_EINVAL: null pointer or bad flags";
-    case MXQ_ESHAPE: return "MXQ_ESHAPE: bad matrix shape";
-    case MXQ_EALIGN: return "MXQ_EALIGN: misaligned pointer or stride";
-    case MXQ_EARCH: return "MXQ_EARCH: device is not sm_103";
-    case MXQ_EWORKSPACE: return "MXQ_EWORKSPACE: workspace missing or too small";
-    case MXQ_ECUDA: return "MXQ_ECUDA: CUDA error";
-    default: return "unknown mxq status";
-  }
-}
-
-size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags) {
-  if (M <= 0 || K <= 0) return 0;
-  if (op == MXQ_OP_NVFP4) return 16;   // one fp32 amax, padded
-  if (op == MXQ_OP_ROWCOL_HOST) return mxq::host_workspace_bytes(M, K);
-  if ((op != MXQ_OP_ROWCOL && op != MXQ_OP_DACT) || !(flags & MXQ_DBIAS)) return 0;
-  const int64_t band = mxq::mx_band_rows(op == MXQ_OP_DACT ? mxq::ACT_DGELU : mxq::ACT_NONE);
-  const int64_t bands = (M + band - 1) / band;
-  return static_cast<size_t>(bands) * static_cast<size_t>(K) * sizeof(float);
-}
-
-mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t flags,
-                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                              float* dbias, void* workspace, size_t workspace_bytes,
-                              uint32_t* dev_err, mxq_stream_t stream) {
+// mx_quantize_rowcol, with the colwise scale row pitch as a parameter.
+mxq_status rowcol_panel(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t flags,
+                        uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                        int64_t scol_ld, float* dbias, void* workspace, size_t workspace_bytes,
+                        uint32_t* dev_err, cudaStream_t stream) {
   const uint32_t known = MXQ_ROWWISE | MXQ_COLWISE | MXQ_DBIAS | MXQ_ACT_GELU_TANH |
                          MXQ_SCALE_RCEIL | MXQ_SCALE_SWIZZLED;
   if (flags & ~known) return MXQ_EINVAL;
@@ -227,6 +205,7 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   a.s_row = s_row;
   a.q_col = q_col;
   a.s_col = s_col;
+  a.scol_ld = scol_ld;
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   if (want_dbias) {
@@ -253,6 +232,41 @@ mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, 
   if (st != MXQ_OK || !want_dbias) return st;
   return from_cuda(mxq::launch_dbias_finalize(a.dbias_ws, a.tiles_m, a.K, dbias, stream));
 }
+}  // namespace mxq
+
+extern "C" {
+
+const char* mxq_status_string(int status) {
+  switch (status) {
+    case MXQ_OK: return "MXQ_OK";
+    case MXQ_EINVAL: return "MXQ_EINVAL: null pointer or bad flags";
+    case MXQ_ESHAPE: return "MXQ_ESHAPE: bad matrix shape";
+    case MXQ_EALIGN: return "MXQ_EALIGN: misaligned pointer or stride";
+    case MXQ_EARCH: return "MXQ_EARCH: device is not sm_103";
+    case MXQ_EWORKSPACE: return "MXQ_EWORKSPACE: workspace missing or too small";
+    case MXQ_ECUDA: return "MXQ_ECUDA: CUDA error";
+    default: return "unknown mxq status";
+  }
+}
+
+size_t mxq_workspace_bytes(int op, int64_t M, int64_t K, uint32_t flags) {
+  if (M <= 0 || K <= 0) return 0;
+  if (op == MXQ_OP_NVFP4) return 16;   // one fp32 amax, padded
+  if (op == MXQ_OP_ROWCOL_HOST) return mxq::host_workspace_bytes(M, K);
+  if ((op != MXQ_OP_ROWCOL && op != MXQ_OP_DACT) || !(flags & MXQ_DBIAS)) return 0;
+  const int64_t band = mxq::mx_band_rows(op == MXQ_OP_DACT ? mxq::ACT_DGELU : mxq::ACT_NONE);
+  const int64_t bands = (M + band - 1) / band;
+  return static_cast<size_t>(bands) * static_cast<size_t>(K) * sizeof(float);
+}
+
+mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t flags,
+                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                              float* dbias, void* workspace, size_t workspace_bytes,
+                              uint32_t* dev_err, mxq_stream_t stream) {
+  return mxq::rowcol_panel(x, M, K, ldx, flags, q_row, s_row, q_col, s_col, M / 32, dbias,
+                           workspace, workspace_bytes, dev_err, stream);
+}
+
 
 mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, uint32_t flags,
                              uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
@@ -290,6 +304,7 @@ mxq_status mx_quantize_gated(const void* x, int64_t M, int64_t N, int64_t ldx, u
   a.s_row = s_row;
   a.q_col = q_col;
   a.s_col = s_col;
+  a.scol_ld = M / 32;
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   mxq::MxMaps maps{};
@@ -356,6 +371,7 @@ mxq_status mx_quantize_dact(const void* grad, const void* x, int64_t M, int64_t 
   a.s_row = s_row;
   a.q_col = q_col;
   a.s_col = s_col;
+  a.scol_ld = M / 32;
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   if (want_dbias) {
@@ -425,6 +441,7 @@ mxq_status mx_quantize_dgated(const void* grad, const void* x, int64_t M, int64_
   a.s_row = s_row;
   a.q_col = q_col;
   a.s_col = s_col;
+  a.scol_ld = M / 32;
   a.dev_err = dev_err;
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   mxq::MxMaps maps{};

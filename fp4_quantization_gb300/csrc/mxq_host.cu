@@ -8,7 +8,12 @@
 // [K][M/32] outputs) as 2-D copies straight into the host layout.  Two sets
 // of device buffers alternate, and the copies in and out run on two
 // library-owned streams, so panel i+1's input copy overlaps panel i's cast
-// and panel i-1's output copies.
+// and panel i-1's output copies.  Row-major colwise scales are the
+// exception: a panel's part is only P / 32 bytes of each [M/32] row, and
+// copies of rows that short run far below the copy engines' rate (64-byte
+// rows: 16 GB/s against 190 GB/s for 2 KiB rows, measured on GB300), so the
+// panels write them into one device copy of the whole [K][M/32] matrix,
+// which leaves in one contiguous copy after the last panel.
 
 #include <cuda_runtime.h>
 
@@ -25,7 +30,10 @@ namespace {
 #endif
 constexpr int64_t kPanelRows = MXQ_HOST_PANEL_ROWS;
 static_assert(kPanelRows % 128 == 0, "panels of whole 128-row bands");
-constexpr int kBuffers = 2;
+#ifndef MXQ_HOST_BUFFERS
+#define MXQ_HOST_BUFFERS 2
+#endif
+constexpr int kBuffers = MXQ_HOST_BUFFERS;
 constexpr int kMaxDevices = 64;
 
 struct HostPipe {
@@ -34,6 +42,7 @@ struct HostPipe {
   cudaEvent_t loaded[kBuffers] = {};   // panel input on the device
   cudaEvent_t done[kBuffers] = {};     // panel quantized
   cudaEvent_t freed[kBuffers] = {};    // panel outputs copied out (buffer reusable)
+  cudaEvent_t tail = nullptr;          // the whole-matrix colwise scales copied out
   bool ready = false;
 };
 HostPipe g_pipes[kMaxDevices];
@@ -49,7 +58,8 @@ mxq_status pipe_on_current_device(HostPipe** out) {
     const unsigned ev = cudaEventDisableTiming;
     if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p.start, ev) != cudaSuccess)
+        cudaEventCreateWithFlags(&p.start, ev) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.tail, ev) != cudaSuccess)
       return MXQ_ECUDA;
     for (int b = 0; b < kBuffers; ++b)
       if (cudaEventCreateWithFlags(&p.loaded[b], ev) != cudaSuccess ||
@@ -87,7 +97,8 @@ int64_t panel_rows(int64_t M) { return M < kPanelRows ? M : kPanelRows; }
 namespace mxq {
 size_t host_workspace_bytes(int64_t M, int64_t K) {
   if (M <= 0 || K <= 0) return 0;
-  return static_cast<size_t>(kBuffers * PanelLayout(panel_rows(M), K).bytes);
+  return static_cast<size_t>(kBuffers * PanelLayout(panel_rows(M), K).bytes +
+                             round256(K * (M / 32)));
 }
 }  // namespace mxq
 
@@ -127,6 +138,10 @@ extern "C" mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t 
   if ((st = cu(cudaStreamWaitEvent(p->h2d, p->start, 0))) != MXQ_OK) return st;
   if ((st = cu(cudaStreamWaitEvent(p->d2h, p->start, 0))) != MXQ_OK) return st;
 
+  // Row-major colwise scales of the whole matrix, [K][M/32], after the panel buffers.
+  const bool whole_scol = col && !tiled;
+  uint8_t* scol_all = ws + kBuffers * L.bytes;
+
   const int64_t panels = (M + P - 1) / P;
   for (int64_t i = 0; i < panels; ++i) {
     const int b = static_cast<int>(i % kBuffers);
@@ -142,9 +157,10 @@ extern "C" mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t 
     if ((st = cu(cudaEventRecord(p->loaded[b], p->h2d))) != MXQ_OK) return st;
     // Cast on the caller's stream.
     if ((st = cu(cudaStreamWaitEvent(stream, p->loaded[b], 0))) != MXQ_OK) return st;
-    st = mx_quantize_rowcol(buf + L.x, rows, K, K, flags, row ? buf + L.q_row : nullptr,
-                            row ? buf + L.s_row : nullptr, col ? buf + L.q_col : nullptr,
-                            col ? buf + L.s_col : nullptr, nullptr, nullptr, 0, nullptr, stream);
+    uint8_t* scol_dev = whole_scol ? scol_all + m0 / 32 : (col ? buf + L.s_col : nullptr);
+    st = mxq::rowcol_panel(buf + L.x, rows, K, K, flags, row ? buf + L.q_row : nullptr,
+                           row ? buf + L.s_row : nullptr, col ? buf + L.q_col : nullptr, scol_dev,
+                           whole_scol ? M / 32 : rows / 32, nullptr, nullptr, 0, nullptr, stream);
     if (st != MXQ_OK) return st;
     if ((st = cu(cudaEventRecord(p->done[b], stream))) != MXQ_OK) return st;
     // Outputs back: rows contiguous, columns as 2-D copies into [K][M].
@@ -164,16 +180,24 @@ extern "C" mxq_status mx_quantize_rowcol_host(const void* x, int64_t M, int64_t 
     if (col) {
       st = cu(cudaMemcpy2DAsync(q_col + m0, M, buf + L.q_col, rows, rows, K,
                                 cudaMemcpyDeviceToHost, p->d2h));
-      // Tiled colwise scales: the panel's tiles of every tile row.
-      if (st == MXQ_OK)
-        st = tiled ? cu(cudaMemcpy2DAsync(s_col + (m0 / 128) * 512, tiles_m * 512, buf + L.s_col,
-                                          ceil_div(rows, 128) * 512, ceil_div(rows, 128) * 512,
-                                          ceil_div(K, 128), cudaMemcpyDeviceToHost, p->d2h))
-                   : cu(cudaMemcpy2DAsync(s_col + m0 / 32, M / 32, buf + L.s_col, rows / 32,
-                                          rows / 32, K, cudaMemcpyDeviceToHost, p->d2h));
+      // Tiled colwise scales: the panel's tiles of every tile row (row-major
+      // ones leave with the whole matrix, below).
+      if (st == MXQ_OK && tiled)
+        st = cu(cudaMemcpy2DAsync(s_col + (m0 / 128) * 512, tiles_m * 512, buf + L.s_col,
+                                  ceil_div(rows, 128) * 512, ceil_div(rows, 128) * 512,
+                                  ceil_div(K, 128), cudaMemcpyDeviceToHost, p->d2h));
       if (st != MXQ_OK) return st;
     }
     if ((st = cu(cudaEventRecord(p->freed[b], p->d2h))) != MXQ_OK) return st;
+  }
+  // The whole-matrix colwise scales, once the last panel is cast (the d2h
+  // stream waited for it above; every earlier cast precedes it on `stream`).
+  if (whole_scol) {
+    if ((st = cu(cudaMemcpyAsync(s_col, scol_all, K * (M / 32), cudaMemcpyDeviceToHost, p->d2h))) !=
+        MXQ_OK)
+      return st;
+    if ((st = cu(cudaEventRecord(p->tail, p->d2h))) != MXQ_OK) return st;
+    if ((st = cu(cudaStreamWaitEvent(stream, p->tail, 0))) != MXQ_OK) return st;
   }
   // The caller's stream continues once the last outputs are on the host.
   for (int b = 0; b < kBuffers && b < panels; ++b)

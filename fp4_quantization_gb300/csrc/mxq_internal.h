@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "mxq.h"
+
 namespace mxq {
 
 // MXFP8: each warp quantizes 32 rows (one colwise block) x 128 columns
@@ -39,6 +41,8 @@ struct MxArgs {
   uint8_t* s_row;
   uint8_t* q_col;
   uint8_t* s_col;
+  int64_t scol_ld;          // bytes between rows of row-major colwise scales (M / 32, or
+                            // the full matrix's when a row panel writes into it)
   float* dbias_ws;          // [tiles_m][K] column sums of each band
   uint32_t* dev_err;
   uint64_t timeout_ns;
@@ -103,8 +107,15 @@ cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two
 cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,
                              int num_sms, cudaStream_t stream);
 cudaError_t launch_nv_global_scale(const float* amax, float* global_scale, cudaStream_t stream);
-// Device workspace of mx_quantize_rowcol_host (two sets of panel buffers).
+// Device workspace of mx_quantize_rowcol_host (two sets of panel buffers and
+// the colwise scales of the whole matrix).
 size_t host_workspace_bytes(int64_t M, int64_t K);
+// mx_quantize_rowcol with the row-major colwise scales written scol_ld bytes
+// apart (a row panel of a wider matrix; scol_ld >= M / 32).
+mxq_status rowcol_panel(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t flags,
+                        uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                        int64_t scol_ld, float* dbias, void* workspace, size_t workspace_bytes,
+                        uint32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, uint32_t* dev_err, cudaStream_t stream);
 
 }  // namespace mxq

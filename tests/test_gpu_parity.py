@@ -67,10 +67,13 @@ def test_mx_rowcol_cta_ranges(M, K, seed, flags):
 
 @pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
-def test_mx_rowcol_host_buffers(flags, pinned):
-    """The host-buffer entry point: three row panels (2048, 2048, 96 rows),
-    ragged K, outputs equal to the device path's byte for byte."""
-    bits = synth.rowcol(M=4192, K=1056, seed=74)
+@pytest.mark.parametrize("M", [4192, 4224], ids=["m4192", "m4224"])
+def test_mx_rowcol_host_buffers(flags, pinned, M):
+    """The host-buffer entry point: three row panels (2048, 2048 and 96 or
+    128 rows; the whole-matrix colwise scale rows are 131 bytes, written byte
+    by byte, or 132, written by 4-byte runs), ragged K, outputs equal to the
+    device path's byte for byte."""
+    bits = synth.rowcol(M=M, K=1056, seed=74)
     x_host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     if pinned:
         x_host = x_host.pin_memory()
