@@ -482,18 +482,23 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
               y[i][2 * p + 1] = v.y;
             }
           }
-          uint32_t cmx[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-          uint32_t rmx[8];
+          // Largest magnitudes of the lane's rows and columns: float max on
+          // |y| (the absolute value is an operand modifier, no instruction of
+          // its own), pairwise trees; non-negative floats order as their bits.
+          auto max8 = [](float a0, float a1, float a2, float a3, float a4, float a5, float a6,
+                         float a7) {
+            return fmaxf(fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))),
+                         fmaxf(fmaxf(fabsf(a4), fabsf(a5)), fmaxf(fabsf(a6), fabsf(a7))));
+          };
+          uint32_t cmx[8], rmx[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            rmx[i] = 0u;
+          for (int i = 0; i < 8; ++i)
+            rmx[i] = __float_as_uint(max8(y[i][0], y[i][1], y[i][2], y[i][3], y[i][4], y[i][5],
+                                          y[i][6], y[i][7]));
 #pragma unroll
-            for (int jc = 0; jc < 8; ++jc) {
-              const uint32_t b = __float_as_uint(y[i][jc]) & 0x7FFFFFFFu;
-              cmx[jc] = max(cmx[jc], b);
-              rmx[i] = max(rmx[i], b);
-            }
-          }
+          for (int jc = 0; jc < 8; ++jc)
+            cmx[jc] = __float_as_uint(max8(y[0][jc], y[1][jc], y[2][jc], y[3][jc], y[4][jc],
+                                           y[5][jc], y[6][jc], y[7][jc]));
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             re[q] = f32_scale_exponent(rmx[2 * q], ceil_f32) |
