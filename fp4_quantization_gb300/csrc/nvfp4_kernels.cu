@@ -18,11 +18,12 @@
 //    rows 8h..8h+7 and columns 8c..8c+7 of those (eight conflict-free
 //    16-byte shared loads).  A 1x16 row block spans lanes c = 2b, 2b+1 and a
 //    16x1 transposed block spans lanes h = 2g, 2g+1: one xor shuffle each.
-//  * Each block scale is computed once: the two lanes of a pair split the
-//    rows (or columns) and swap the reciprocals with one shuffle.  A 16x16
-//    block spans the four lanes (h pair) x (c pair): its amax takes the
-//    xor-1 and xor-8 shuffles and every lane looks its one scale up.  The scale
-//    arithmetic is IEEE fp32 with explicit rounding intrinsics in the fixed
+//  * Block scales come from a per-CTA table (NvScaleTables): both lanes of a
+//    pair look up all eight blocks they multiply (a clamp and one shared
+//    load each, cheaper than swapping reciprocals by shuffle), and each
+//    stages the codes of its four.  A 16x16 block spans the four lanes (h
+//    pair) x (c pair): its amax takes the xor-1 and xor-8 shuffles and every
+//    lane looks its one scale up.  The table holds the scale arithmetic, IEEE fp32 with explicit rounding intrinsics in the fixed
 //    order (b / 6) / G -> E4M3 -> value * G -> 1 / d; each element then
 //    takes one multiply by that reciprocal (two per mul.rn.f32x2; no
 //    per-element division, as in torchao PR #12 "Multiply with inverse
@@ -347,7 +348,7 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
     // ---- rowwise: block scales (split over the c pair), codes, scale bytes --
     if constexpr (ROW) {
-      const int mine = c & 1;               // this lane scales rows 4*mine .. 4*mine+3
+      const int mine = c & 1;               // this lane stages the codes of rows 4*mine .. 4*mine+3
       uint32_t rcode[4];
       float rinv[8];
       if constexpr (TWO_D) {
@@ -359,20 +360,13 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           rm[q] = absmax_bf16x2(rm[q], __shfl_xor_sync(0xFFFFFFFFu, rm[q], 1));
-        float rinv_own[4], rinv_oth[4];
+        // Both lanes of the pair look up all eight row blocks (a lookup is
+        // one clamp and one shared load); each stages the codes of its four.
+        uint32_t code8[8];
 #pragma unroll
-        for (int tq = 0; tq < 4; ++tq) {
-          const uint32_t pair = mine ? rm[2 + (tq >> 1)] : rm[tq >> 1];
-          tabs.lookup(mag16(pair, tq & 1), rcode[tq], rinv_own[tq]);
-        }
+        for (int i = 0; i < 8; ++i) tabs.lookup(mag16(rm[i >> 1], i & 1), code8[i], rinv[i]);
 #pragma unroll
-        for (int tq = 0; tq < 4; ++tq)
-          rinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, rinv_own[tq], 1);
-#pragma unroll
-        for (int tq = 0; tq < 4; ++tq) {
-          rinv[tq] = mine ? rinv_oth[tq] : rinv_own[tq];
-          rinv[4 + tq] = mine ? rinv_own[tq] : rinv_oth[tq];
-        }
+        for (int tq = 0; tq < 4; ++tq) rcode[tq] = mine ? code8[4 + tq] : code8[tq];
       }
       // Codes of row i: 8 values -> 4 bytes at k / 2 = 4c within this step.
       const int slot4 = tk & 3;
@@ -408,7 +402,7 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
     // ---- transposed: block scales (split over the h pair), codes, scales ----
     if constexpr (COL) {
-      const int mine = h & 1;               // this lane scales columns 4*mine .. 4*mine+3
+      const int mine = h & 1;               // this lane stages the codes of columns 4*mine .. 4*mine+3
       uint32_t tcode[4];
       float tinv[8];
       if constexpr (TWO_D) {
@@ -420,20 +414,13 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
         for (int p = 0; p < 4; ++p)
           cm[p] = absmax_bf16x2(cm[p], __shfl_xor_sync(0xFFFFFFFFu, cm[p], 8));
-        float tinv_own[4], tinv_oth[4];
+        // Both lanes of the pair look up all eight column blocks; each
+        // stages the codes of its four.
+        uint32_t code8[8];
 #pragma unroll
-        for (int tq = 0; tq < 4; ++tq) {
-          const uint32_t pair = mine ? cm[2 + (tq >> 1)] : cm[tq >> 1];
-          tabs.lookup(mag16(pair, tq & 1), tcode[tq], tinv_own[tq]);
-        }
+        for (int j = 0; j < 8; ++j) tabs.lookup(mag16(cm[j >> 1], j & 1), code8[j], tinv[j]);
 #pragma unroll
-        for (int tq = 0; tq < 4; ++tq)
-          tinv_oth[tq] = __shfl_xor_sync(0xFFFFFFFFu, tinv_own[tq], 8);
-#pragma unroll
-        for (int tq = 0; tq < 4; ++tq) {
-          tinv[tq] = mine ? tinv_oth[tq] : tinv_own[tq];
-          tinv[4 + tq] = mine ? tinv_own[tq] : tinv_oth[tq];
-        }
+        for (int tq = 0; tq < 4; ++tq) tcode[tq] = mine ? code8[4 + tq] : code8[tq];
       }
       // Codes of column jc: 8 rows -> 4 bytes at m / 2 = 16 * warp + 4h.
 #pragma unroll
