@@ -23,8 +23,9 @@
 //    load each, cheaper than swapping reciprocals by shuffle), and each
 //    stages the codes of its four.  A 16x16 block spans the four lanes (h
 //    pair) x (c pair): its amax takes the xor-1 and xor-8 shuffles and every
-//    lane looks its one scale up.  The table holds the scale arithmetic, IEEE fp32 with explicit rounding intrinsics in the fixed
-//    order (b / 6) / G -> E4M3 -> value * G -> 1 / d; each element then
+//    lane looks its one scale up.  The table holds the scale arithmetic,
+//    IEEE fp32 with explicit rounding intrinsics in the fixed order
+//    (b / 6) / G -> E4M3 -> value * G -> 1 / d; each element then
 //    takes one multiply by that reciprocal (two per mul.rn.f32x2; no
 //    per-element division, as in torchao PR #12 "Multiply with inverse
 //    scale in loop instead of dividing", rationale) and
