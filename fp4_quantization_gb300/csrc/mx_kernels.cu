@@ -666,20 +666,23 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
 
       // ---- dbias: column sums of the warp's 16 rows, pairwise ----------------
       if constexpr (DBIAS) {
+        // Columns 2p and 2p + 1 together (add.rn.f32x2: two independent fp32
+        // sums, the same pairwise order per column).
         float s16[8];
 #pragma unroll
-        for (int jc = 0; jc < 8; ++jc) {
-          float v[8];
+        for (int p = 0; p < 4; ++p) {
+          float2 v[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 pr = pair_at(i, jc >> 1);
-            v[i] = (jc & 1) ? pr.y : pr.x;
-          }
+          for (int i = 0; i < 8; ++i) v[i] = pair_at(i, p);
 #pragma unroll
           for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
-            for (int i = 0; i < w; ++i) v[i] = v[i] + v[i + w];
-          s16[jc] = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 16);
+            for (int i = 0; i < w; ++i) v[i] = add_f32x2(v[i], v[i + w]);
+          const float2 o = make_float2(__shfl_xor_sync(0xFFFFFFFFu, v[0].x, 16),
+                                       __shfl_xor_sync(0xFFFFFFFFu, v[0].y, 16));
+          const float2 t = add_f32x2(v[0], o);
+          s16[2 * p] = t.x;
+          s16[2 * p + 1] = t.y;
         }
         // Two 16-byte stores per lane, 16 lanes side by side (no conflicts).
         if (h == 0) {

@@ -174,10 +174,11 @@ MXQ_API mxq_status mx_quantize_rowcol_dbias_noalloc(const void* x, int64_t M, in
  *
  * The same cast (plain, no dbias or activation) of x in row panels of up to
  * 2048 rows: each panel is copied to the device, quantized, and its outputs
- * copied back (colwise codes and scales as 2-D copies into the [K][M] and
- * [K][M/32] host layouts); two sets of device buffers alternate and the
- * copies run on two library-owned streams, so copies in, casts and copies
- * out of consecutive panels overlap.
+ * copied back (colwise codes as 2-D copies into the [K][M] host layout;
+ * row-major colwise scales gathered on the device for the whole matrix and
+ * copied back once, after the last panel); two sets of device buffers
+ * alternate and the copies run on two library-owned streams, so copies in,
+ * casts and copies out of consecutive panels overlap.
  *
  *   x, q_row, s_row, q_col, s_col  host memory with the layouts of
  *           mx_quantize_rowcol; page-locked memory lets the copies run
