@@ -863,27 +863,45 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
   if (tid == 0) bulk_wait_all();
 }
 
-// dbias[k] = sum over bands of the band sums: four threads per column each
-// add a quarter of the bands in band order, then the quarters are added as
-// (q0 + q1) + (q2 + q3) -- a fixed order, so the result does not depend on
-// scheduling.
+// dbias[k] = sum over bands of the band sums.  A block takes 64 columns with
+// 256 threads: thread (g, q) adds columns 4q .. 4q + 3 (one 16-byte load
+// per band) over band group g (bands g * per .. g * per + per - 1, in band
+// order), and the 16 group sums are then added pairwise in a fixed tree
+// (g + 8, g + 4, g + 2, g + 1) -- a fixed order, so the result does not
+// depend on scheduling; all of a thread's loads are independent, so the
+// pass costs about one memory latency.
 constexpr int kFinalizeCols = 64;
-__global__ void __launch_bounds__(4 * kFinalizeCols)
+constexpr int kFinalizeGroups = 16;
+__global__ void __launch_bounds__(kFinalizeGroups * kFinalizeCols / 4)
 dbias_finalize_kernel(const float* __restrict__ ws, int bands, int K, float* __restrict__ dbias) {
-  __shared__ float part[4][kFinalizeCols];
+  __shared__ float4 part[kFinalizeGroups][kFinalizeCols / 4];
   grid_dependency_wait();   // the band sums of the quantize grid before it
-  const int kc = threadIdx.x % kFinalizeCols, q = threadIdx.x / kFinalizeCols;
-  const int k = blockIdx.x * kFinalizeCols + kc;
-  const int per = (bands + 3) / 4;
-  const int b0 = q * per, b1 = min(bands, b0 + per);
-  float sum = 0.0f;
+  const int q = threadIdx.x % (kFinalizeCols / 4), g = threadIdx.x / (kFinalizeCols / 4);
+  const int k = blockIdx.x * kFinalizeCols + 4 * q;   // K is a multiple of 32
+  const int per = (bands + kFinalizeGroups - 1) / kFinalizeGroups;
+  const int b0 = g * per, b1 = min(bands, b0 + per);
+  float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (k < K) {
 #pragma unroll 4
-    for (int p = b0; p < b1; ++p) sum += ws[static_cast<size_t>(p) * K + k];
+    for (int b = b0; b < b1; ++b) {
+      const float4 v = *reinterpret_cast<const float4*>(ws + static_cast<size_t>(b) * K + k);
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
   }
-  part[q][kc] = sum;
+  part[g][q] = sum;
   __syncthreads();
-  if (q == 0 && k < K) dbias[k] = (part[0][kc] + part[1][kc]) + (part[2][kc] + part[3][kc]);
+#pragma unroll
+  for (int w = kFinalizeGroups / 2; w >= 1; w >>= 1) {
+    if (g < w) {
+      const float4 a = part[g][q], b = part[g + w][q];
+      part[g][q] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    }
+    __syncthreads();
+  }
+  if (g == 0 && k < K) *reinterpret_cast<float4*>(dbias + k) = part[0][q];
 }
 
 // ---------------------------------------------------------------------------
@@ -1090,7 +1108,7 @@ cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbia
   // on the stream, so its launch overlaps that grid's last steps.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((K + kFinalizeCols - 1) / kFinalizeCols);
-  cfg.blockDim = dim3(4 * kFinalizeCols);
+  cfg.blockDim = dim3(kFinalizeGroups * kFinalizeCols / 4);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
