@@ -67,12 +67,12 @@ def test_mx_rowcol_cta_ranges(M, K, seed, flags):
 
 @pytest.mark.parametrize("flags", [BOTH, mxq.ROWWISE, mxq.COLWISE], ids=["both", "row", "col"])
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
-@pytest.mark.parametrize("M", [4192, 4224], ids=["m4192", "m4224"])
+@pytest.mark.parametrize("M", [4192, 4224, 8288], ids=["m4192", "m4224", "m8288"])
 def test_mx_rowcol_host_buffers(flags, pinned, M):
     """The host-buffer entry point: three row panels (2048, 2048 and 96 or
     128 rows; the whole-matrix colwise scale rows are 131 bytes, written byte
-    by byte, or 132, written by 4-byte runs), ragged K, outputs equal to the
-    device path's byte for byte."""
+    by byte, or 132, written by 4-byte runs) or five (4 x 2048 + 96), ragged
+    K, outputs equal to the device path's byte for byte."""
     bits = synth.rowcol(M=M, K=1056, seed=74)
     x_host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     if pinned:
@@ -183,13 +183,14 @@ def test_mx_tiled_scales_fused_paths():
     with pytest.raises(mxq.MxqError):
         mxq.mx_quantize_dgated(to_device(synth.gelu(M=64, K=96, seed=92)),
                                to_device(synth.swiglu(M=64, N=96, seed=93)), BOTH | mxq.SCALE_SWIZZLED)
-    hb = synth.rowcol(M=4192, K=1056, seed=94)
-    xh = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory()
-    out = mxq.mx_quantize_rowcol_host(xh, BOTH | mxq.SCALE_SWIZZLED)
-    torch.cuda.synchronize()
-    ref = oracle.mx_quantize(hb, BOTH | oracle.SCALE_SWIZZLED)
-    for key in ref:
-        assert_equal_bytes(out[key].numpy(), ref[key], f"tiled host {key}")
+    for M in (4192, 8288):   # three and five row panels
+        hb = synth.rowcol(M=M, K=1056, seed=94)
+        xh = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory()
+        out = mxq.mx_quantize_rowcol_host(xh, BOTH | mxq.SCALE_SWIZZLED)
+        torch.cuda.synchronize()
+        ref = oracle.mx_quantize(hb, BOTH | oracle.SCALE_SWIZZLED)
+        for key in ref:
+            assert_equal_bytes(out[key].numpy(), ref[key], f"tiled host M={M} {key}")
 
 
 def test_mx_rowcol_strided_input():
