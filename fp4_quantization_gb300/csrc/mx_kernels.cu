@@ -239,6 +239,13 @@ __device__ __forceinline__ uint32_t f32_scale_exponent(uint32_t b, uint32_t ceil
   return (b + ceil_add) >> 23;
 }
 
+// Largest of three floats (one three-input max instruction).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void bar_sync_cta(int threads) {
   asm volatile("bar.sync 1, %0;" :: "r"(threads) : "memory");
 }
@@ -484,11 +491,12 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
           }
           // Largest magnitudes of the lane's rows and columns: float max on
           // |y| (the absolute value is an operand modifier, no instruction of
-          // its own), pairwise trees; non-negative floats order as their bits.
+          // its own), three-input max trees (four instructions per eight
+          // values); non-negative floats order as their bits.
           auto max8 = [](float a0, float a1, float a2, float a3, float a4, float a5, float a6,
                          float a7) {
-            return fmaxf(fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))),
-                         fmaxf(fmaxf(fabsf(a4), fabsf(a5)), fmaxf(fabsf(a6), fabsf(a7))));
+            return fmax3(fmax3(fabsf(a0), fabsf(a1), fabsf(a2)), fmax3(fabsf(a3), fabsf(a4), fabsf(a5)),
+                         fmaxf(fabsf(a6), fabsf(a7)));
           };
           uint32_t cmx[8], rmx[8];
 #pragma unroll
