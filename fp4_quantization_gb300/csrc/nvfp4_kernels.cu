@@ -50,8 +50,12 @@ namespace {
 #ifndef MXQ_NV_STAGES
 #define MXQ_NV_STAGES 3
 #endif
+// L2 policy of the input copies: 0 none, 1 evict-last, 2 evict-normal.
+// Measured on GB300 (2D 8192^2 / 16384x8192): none 41.7 / 75.9 us,
+// evict-last 43.1 / 76.4, evict-normal 43.0 / 76.3; ring slots 2 and 4 were
+// slower than 3.
 #ifndef MXQ_NV_LOAD_HINT
-#define MXQ_NV_LOAD_HINT 1
+#define MXQ_NV_LOAD_HINT 0
 #endif
 
 constexpr int NV_WARPS = 8;
@@ -250,7 +254,8 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
     mbar_arrive_expect_tx(bar0 + 8 * s, NV_STAGE_BYTES);
 #if MXQ_NV_LOAD_HINT
     tma_load_2d_hint(sbase + s * NV_STAGE_BYTES, &tmap_x, tk * NV_STEP_K, band * NV_BAND,
-                     bar0 + 8 * s, l2_policy_evict_last());
+                     bar0 + 8 * s,
+                     MXQ_NV_LOAD_HINT == 2 ? l2_policy_evict_normal() : l2_policy_evict_last());
 #else
     tma_load_2d(sbase + s * NV_STAGE_BYTES, &tmap_x, tk * NV_STEP_K, band * NV_BAND, bar0 + 8 * s);
 #endif
