@@ -502,3 +502,45 @@ def test_non_default_stream():
     s.synchronize()
     ref = oracle.mx_quantize(bits, BOTH)
     assert_equal_bytes(host(out["q_row"]), ref["q_row"], "stream q_row")
+
+
+def test_two_launch_paths_back_to_back():
+    """The dbias finalize and the NVFP4 quantize after its amax pass are
+    launched as programmatic dependents of the grid before them: calls on two
+    inputs, alternated without synchronising and sharing one workspace, each
+    see only their own first grid's results."""
+    a_bits = synth.dbias(M=2048, K=1024, seed=60)
+    b_bits = synth.dbias(M=2048, K=1024, seed=61)
+    a, b = to_device(a_bits), to_device(b_bits)
+    flags = BOTH | mxq.DBIAS
+    ws = torch.empty(mxq.mxq_workspace_bytes(mxq.OP_ROWCOL, 2048, 1024, flags), dtype=torch.uint8,
+                     device="cuda")
+    out_a = mxq.mx_quantize_rowcol(a, flags, workspace=ws)
+    out_b = mxq.mx_quantize_rowcol(b, flags, workspace=ws)
+    for _ in range(3):
+        mxq.mx_quantize_rowcol(a, flags, workspace=ws, **out_a)
+        mxq.mx_quantize_rowcol(b, flags, workspace=ws, **out_b)
+    torch.cuda.synchronize()
+    for bits, out in ((a_bits, out_a), (b_bits, out_b)):
+        ref = oracle.mx_quantize(bits, flags)
+        for key in ("q_row", "s_row", "q_col", "s_col"):
+            assert_equal_bytes(host(out[key]), ref[key], f"back-to-back dbias {key}")
+        err = np.abs(host(out["dbias"]).astype(np.float64) - ref["dbias"].astype(np.float64))
+        assert np.all(err <= _dbias_tolerance(bits)), f"back-to-back dbias max err {err.max()}"
+
+    c_bits = synth.nvfp4(M=512, K=1024, seed=62)
+    d_f32 = synth.bf16_bits_to_f32(synth.nvfp4(M=512, K=1024, seed=63)) * np.float32(8.0)
+    d_bits = (d_f32.view(np.uint32) >> 16).astype(np.uint16)   # exact: x 8 keeps bf16 values
+    c, d = to_device(c_bits), to_device(d_bits)
+    nws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    out_c = mxq.nvfp4_quantize_transpose(c, BOTH, workspace=nws)
+    out_d = mxq.nvfp4_quantize_transpose(d, BOTH, workspace=nws)
+    for _ in range(3):
+        mxq.nvfp4_quantize_transpose(c, BOTH, workspace=nws, **out_c)
+        mxq.nvfp4_quantize_transpose(d, BOTH, workspace=nws, **out_d)
+    torch.cuda.synchronize()
+    for bits, out in ((c_bits, out_c), (d_bits, out_d)):
+        ref = oracle.nvfp4_quantize(bits)
+        assert host(out["global_scale"])[0] == np.float32(ref["global_scale"])
+        for key in ("q_row", "s_row", "q_t", "s_t"):
+            assert_equal_bytes(host(out[key]), ref[key], f"back-to-back nvfp4 {key}")
