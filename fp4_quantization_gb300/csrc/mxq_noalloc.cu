@@ -19,7 +19,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "mxq.h"
 
@@ -31,24 +30,19 @@ constexpr size_t kScratchBytes = size_t(8) << 20;   // 8 MiB
 // cudaGetSymbolAddress, never a device address.
 static __device__ __align__(256) unsigned char g_dbias_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mutex;
-
-// Device address of the scratch array on the current device, looked up on
-// the first call made with that device current.
+// Device address of the scratch array in the current context.  Looked up on
+// every call, not cached: after cudaDeviceReset, or with another context
+// current for the same device, the module is loaded again and the array may
+// sit at another address.  The lookup is a host-side table search once the
+// module is loaded; the first call on a device loads it, which is why that
+// first call must come before any stream capture begins.
 mxq_status scratch_on_current_device(void** addr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MXQ_ECUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MXQ_EARCH;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dbias_scratch) != cudaSuccess || p == nullptr)
-      return MXQ_ECUDA;
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dbias_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();   // a failed lookup leaves no error behind for later calls
+    return MXQ_ECUDA;
   }
-  *addr = g_scratch_addr[dev];
+  *addr = p;
   return MXQ_OK;
 }
 

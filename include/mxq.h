@@ -30,6 +30,8 @@
  *    *dev_err, waits (bounded) for its own copies in flight and exits
  *    without writing the remaining tiles.  The library never clears
  *    *dev_err; the caller zeroes it and reads it back after the stream.
+ *    When *dev_err is nonzero after a call, every output of that call
+ *    (codes, scales, dbias, the global scale) is undefined.
  *  * Alignment: `x`, every output and the workspace 16-byte aligned, `ldx`
  *    a multiple of 8.  Violations return MXQ_EALIGN.
  *  * The device must be compute capability 10.3 (GB300): else MXQ_EARCH.
@@ -154,11 +156,16 @@ MXQ_API mxq_status mx_quantize_rowcol(const void* x, int64_t M, int64_t K, int64
  *   - Limit: shapes needing more than 8 MiB of band sums
  *     (mxq_workspace_bytes(MXQ_OP_ROWCOL, M, K, MXQ_DBIAS) > 8 MiB, e.g.
  *     more than 16384 x 16384) return MXQ_EWORKSPACE; nothing is enqueued.
- *   - The first call made with a device current looks up the array's device
- *     address; make that first call before any stream capture begins.
+ *   - Every call looks up the array's device address in the current
+ *     context; the first call with a device current also loads the
+ *     library's device code there, so make that first call before any
+ *     stream capture begins.
  *   - All calls share the array.  Nothing in it needs clearing (every value
  *     read is written earlier in the same call), but calls that overlap on
- *     the GPU race on it: order them, e.g. on one stream.
+ *     the GPU race on it: order them, e.g. on one stream.  Calls queued one
+ *     after another on one stream do not overlap.
+ *   - As for every entry point, the outputs are undefined when the call
+ *     reports a timeout through *dev_err.
  *   - It never calls cudaMalloc, cudaFree or any allocating routine.
  */
 MXQ_API mxq_status mx_quantize_rowcol_dbias_noalloc(const void* x, int64_t M, int64_t K,

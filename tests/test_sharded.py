@@ -14,7 +14,7 @@ import torch.multiprocessing as mp
 import oracle
 import synth
 
-sharded = pytest.importorskip("fp4_quantization_gb300.sharded")
+from fp4_quantization_gb300 import sharded  # noqa: E402
 
 
 def _free_port():
