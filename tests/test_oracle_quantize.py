@@ -321,6 +321,32 @@ def test_dgated_halves():
         np.testing.assert_array_equal(out["s_col"][64:], fwd["s_col"])
 
 
+def test_dgated_products_compose():
+    """The gated backward with grad and up that vary per element: powers of
+    two (grad in {+-0.5, 2, 4}, up in {+-0.25, 2, 8}), so each product is an
+    exact rescaling of the separately pinned scalar.  Rebuilt here:
+    d gate = grad * up * act'(gate) and d up = grad * act(gate), then the
+    blocks from the pinned encoders.  Dropping up or grad from either half,
+    or taking act'(up), changes these blocks."""
+    M, N = 64, 64
+    gate = synth.gelu(M=M, K=N, seed=21)
+    rng = np.random.default_rng(22)
+    gvals = rng.choice(np.array([0.5, -0.5, 2.0, 4.0], np.float32), size=(M, N))
+    uvals = rng.choice(np.array([0.25, -0.25, 2.0, 8.0], np.float32), size=(M, N))
+    grad, up = bf16(gvals), bf16(uvals)
+    x = np.hstack([gate, up])
+    gf = synth.bf16_bits_to_f32(gate)
+    for act, dfn, fn in ((oracle.ACT_SILU, oracle.dsilu, lambda v: oracle.swiglu(v, 1.0)),
+                         (oracle.ACT_GELU_TANH, oracle.dgelu_tanh, oracle.gelu_tanh)):
+        out = oracle.mx_quantize_dgated(grad, x, N, act)
+        y = np.empty((M, 2 * N), np.float32)
+        for m in range(M):
+            for n in range(N):
+                y[m, n] = gvals[m, n] * uvals[m, n] * np.float32(dfn(gf[m, n]))
+                y[m, N + n] = gvals[m, n] * np.float32(fn(gf[m, n]))
+        _check_blocks(y.astype(np.float64), out)
+
+
 def _check_blocks(y, out):
     M, K = y.shape
     for m in range(M):
