@@ -260,9 +260,14 @@ PAGES_GB200_COLD_US = {
 }
 
 
-def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None):
+# Kernel launches per call of each row (the rest launch one kernel).
+ROW_LAUNCHES = {"dbias_rowcol_8192x8192": 2, "dbias_dgelu_rowcol_8192x14336": 2,
+                "nvfp4_rowtrans_16384x8192": 2}
+
+
+def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None, clock_index=0):
     """The other hot-path variants, each on its own workload (only the one
-    named `only` when given)."""
+    named `only` when given), `steps` timed calls each."""
     out = {}
     cases = [
         ("rowcol_8192x28672", lambda: synth.rowcol(M=8192, K=28672),
@@ -336,17 +341,22 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
             keep["workspace"] = torch.empty(
                 max(16, mxq.mxq_workspace_bytes(mxq.OP_DACT, 8192, 14336, 7)), dtype=torch.uint8,
                 device=device)
-        total, per_call, _ = time_device(lambda: call(x, keep), steps, warmup, world, stream)
+        with ClockSampler(clock_index) as clocks:
+            total, per_call, _ = time_device(lambda: call(x, keep), steps, warmup, world, stream)
         # Device time per call (events around each call); the loop time per
         # call beside it also holds the host's time between calls, which
-        # the shortest calls do not cover.
-        avg_ms = statistics.mean(per_call)
-        gbs = nbytes / (avg_ms * 1e-3) / 1e9
-        launches = 2 if (name.startswith("dbias") or name.startswith("nvfp4_rowtrans_16")) else 1
-        out[name] = {"GB_per_s": round(gbs, 1), "us_per_call": round(avg_ms * 1e3, 2),
+        # the shortest calls do not cover.  GB/s and the fraction of peak
+        # use the median call.
+        med_ms = statistics.median(per_call)
+        gbs = nbytes / (med_ms * 1e-3) / 1e9
+        launches = ROW_LAUNCHES.get(name, 1)
+        out[name] = {"GB_per_s": round(gbs, 1), "us_per_call": round(med_ms * 1e3, 2),
+                     "us_min": round(min(per_call) * 1e3, 2),
+                     "us_mean": round(statistics.mean(per_call) * 1e3, 2),
+                     "calls": steps,
                      "loop_us_per_call": round(total / steps * 1e3, 2),
                      "bytes_per_call": nbytes, "frac_of_hbm_peak": round(gbs / peak, 4),
-                     "launches_per_call": launches}
+                     "launches_per_call": launches, "clocks": clocks.summary()}
         if name.startswith("nvfp4_rowtrans_16"):
             out[name]["note"] = ("bytes exclude the tensor-amax pass (a second 256 MiB read), "
                                  "time includes it")
@@ -361,6 +371,19 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
         del x, first, keep
         torch.cuda.empty_cache()
     return out
+
+
+def copy_ceiling(device, steps, stream, elems=256 * 2 ** 20):
+    """torch's device-to-device copy of `elems` bf16 values (read + write
+    bytes), timed with events: median and best over `steps` calls."""
+    a = torch.empty(elems, dtype=torch.bfloat16, device=device).normal_()
+    b = torch.empty_like(a)
+    _, per_call, _ = time_device(lambda: b.copy_(a), max(3, steps), 3, 1, stream)
+    nbytes = 2 * a.numel() * a.element_size()
+    med = statistics.median(per_call)
+    return {"bytes_per_call": nbytes, "us_per_call": round(med * 1e3, 2),
+            "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 1),
+            "best_GB_per_s": round(nbytes / (min(per_call) * 1e-3) / 1e9, 1)}
 
 
 def cold_l2_measure(fn, steps, stream, device, flush_bytes=512 * 2 ** 20):
@@ -434,20 +457,21 @@ def oracle_on_threads(bits, flags, threads):
         return time.perf_counter() - t0
 
 
-def cpu_baseline(rows=4096, K=16384):
-    """The oracle as it stands on the first `rows` rows of the workload (same
-    seeded generator), on every host core (row panels, one thread each) and,
-    for reference, on one thread."""
-    bits = synth.rowcol(M=rows, K=K)
+def cpu_baseline(bits):
+    """The oracle as it stands on the whole workload (the bench's own input),
+    on every host core (row panels, one thread each) -- the same definition
+    as the reference arm's step -- and, for context, on one thread over the
+    first 1024 rows."""
+    rows, K = bits.shape
     threads = host_threads()
     dt = oracle_on_threads(bits, 3, threads)
-    dt1 = oracle_on_threads(bits[:rows // 4], 3, 1) * 4
+    dt1 = oracle_on_threads(bits[:1024], 3, 1) * (rows / 1024)
     gbs = mx_bytes(rows, K) / dt / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {rows} of 16384 rows ({rows}x{K} bf16), rowwise+colwise, "
+            "sample": f"all {rows} rows ({rows}x{K} bf16, the bench's input), rowwise+colwise, "
                       f"{dt:.2f} s on {threads} host threads (row panels)",
             "one_thread": {"value": round(mx_bytes(rows, K) / dt1 / 1e9, 4), "unit": "GB/s",
-                           "sample": f"first {rows // 4} rows on 1 thread, scaled x4"}}
+                           "sample": f"first 1024 rows on 1 thread, scaled x{rows / 1024:g}"}}
 
 
 def gpu_arm(args):
@@ -458,10 +482,18 @@ def gpu_arm(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
     peak, peak_kind = measured_peaks()
+    clock_index = local if world > 1 else int(os.environ.get("MXQ_NVML_INDEX", "0"))
+    if args.only == "copy_ceiling":
+        # The denominator's own kind of kernel (torch's device copy) on a
+        # 512 MiB bf16 buffer: for profiling it beside the cast in the same
+        # units.  Not part of the hot path.
+        print(json.dumps({"only": args.only, "copy": copy_ceiling(device, args.steps, stream)}),
+              flush=True)
+        return
     if args.only:
         # One hot-path variant alone (profiling runs); no headline line.
         rows = rows_measurements(mxq, device, args.steps, args.warmup, world, stream, peak,
-                                 only=args.only)
+                                 only=args.only, clock_index=clock_index)
         if rank == 0:
             print(json.dumps({"only": args.only, "rows": rows}), flush=True)
         return
@@ -474,7 +506,7 @@ def gpu_arm(args):
     def step():
         mxq.mx_quantize_rowcol(x, mxq.ROWWISE | mxq.COLWISE, **outs)
 
-    with ClockSampler(local if world > 1 else int(os.environ.get("MXQ_NVML_INDEX", "0"))) as clocks:
+    with ClockSampler(clock_index) as clocks:
         total_ms, per_call, total_max = time_device(step, args.steps, args.warmup, world, stream)
     avg_call_ms = statistics.mean(per_call)
     value = nbytes * world / (total_max * 1e-3 / args.steps) / 1e9
@@ -510,8 +542,8 @@ def gpu_arm(args):
                          "GB_per_s": round(nbytes / (cold_ms * 1e-3) / 1e9, 1),
                          "how": "median over calls, 512 MiB zeroed before each (untimed)"}
     if args.rows:
-        result["rows"] = rows_measurements(mxq, device, max(5, args.steps // 4), max(3, args.warmup),
-                                           world, stream, peak)
+        result["rows"] = rows_measurements(mxq, device, max(50, args.steps), max(3, args.warmup),
+                                           world, stream, peak, clock_index=clock_index)
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
         ms, h2d, d2h = e2e_measure(mxq, bits, device, e2e_steps, 3, stream)
@@ -519,7 +551,7 @@ def gpu_arm(args):
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": round(ms, 4), "steps": e2e_steps}
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(rows=args.cpu_rows)
+        result["cpu_baseline"] = cpu_baseline(bits)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -585,7 +617,6 @@ def main():
     p.add_argument("--no-rows", dest="rows", action="store_false")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-rows", type=int, default=4096)
     p.add_argument("--only", default=None,
                    help="time just this variant of the 'rows' object (profiling runs)")
     p.add_argument("--M", type=int, default=16384,
