@@ -319,7 +319,7 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
          lambda x, o: mxq.bf16_amax(x, **o), 16384 * 8192 * 2 + 4, {}),
     ]
     for name, gen, call, nbytes, _ in cases:
-        if only is not None and name != only:
+        if only is not None and name not in only.split(","):
             continue
         data = gen()
         x = (tuple(to_device(d, device) for d in data) if isinstance(data, tuple)
@@ -618,7 +618,8 @@ def main():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--only", default=None,
-                   help="time just this variant of the 'rows' object (profiling runs)")
+                   help="time just these variants of the 'rows' object, comma-separated "
+                        "(profiling runs)")
     p.add_argument("--M", type=int, default=16384,
                    help="rows of the timed cast (16384 for the headline number)")
     p.add_argument("--K", type=int, default=16384, help="columns of the timed cast")

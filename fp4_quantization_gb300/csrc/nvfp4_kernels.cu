@@ -37,7 +37,9 @@
 //    Both layouts keep the shared-memory stores free of bank conflicts.
 //  * Rowwise scale bytes of eight steps are gathered into one 32-byte
 //    sector per row; transposed scale bytes leave as 16 bytes per column
-//    per step.
+//    per step.  The partial groups at the ends of a CTA's range leave in
+//    whole sectors too (codes: thread pairs, 16 bytes each, one instruction
+//    per sector; scales: one request per row run).
 
 #include <cfloat>
 
@@ -204,18 +206,31 @@ __device__ __forceinline__ void nv_flush_rscales(const NvArgs& a, uint32_t sbase
   const int kb0 = (tk - slot8) * (NV_STEP_K / 16);
   // Two 16-byte halves: every row start must be 16-byte aligned.
   const bool full = first == 0 && slot8 == 7 && (nkb & 15) == 0;
-  for (int it = tid; it < 2 * NV_BAND; it += NV_WARPS * 32) {
-    const int rr = it >> 1, half = it & 1;
+  if (full) {
+    for (int it = tid; it < 2 * NV_BAND; it += NV_WARPS * 32) {
+      const int rr = it >> 1, half = it & 1;
+      const int row = band * NV_BAND + rr;
+      if (row >= a.M) continue;
+      const uint32_t s16 = sbase + NV_OFF_RSC + rr * NV_RSC_PITCH + 16 * half;
+      stg128(a.s_row + static_cast<size_t>(row) * nkb + kb0 + 16 * half, lds32(s16),
+             lds32(s16 + 4), lds32(s16 + 8), lds32(s16 + 12));
+    }
+    return;
+  }
+  // A partial group: eight neighbouring threads per row, thread w writing
+  // the 4 bytes of slot w when the group has them, so the row's run leaves
+  // as one request.  A slot past the last column (K % 64 == 32) has 2 bytes.
+  const int b_end = nkb - kb0;   // scale bytes of this group inside the row
+  for (int it = tid; it < 8 * NV_BAND; it += NV_WARPS * 32) {
+    const int rr = it >> 3, w = it & 7;
     const int row = band * NV_BAND + rr;
-    if (row >= a.M) continue;
-    uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0;
-    const uint32_t src = sbase + NV_OFF_RSC + rr * NV_RSC_PITCH;
-    if (full) {
-      const uint32_t s16 = src + 16 * half;
-      stg128(dst + 16 * half, lds32(s16), lds32(s16 + 4), lds32(s16 + 8), lds32(s16 + 12));
-    } else if (half == 0) {
-      const int b_end = min((slot8 + 1) * 4, nkb - kb0);
-      copy_run_to_global(dst + first * 4, src + first * 4, b_end - first * 4);
+    if (row >= a.M || w < first || w > slot8 || 4 * w >= b_end) continue;
+    uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + kb0 + 4 * w;
+    const uint32_t src = sbase + NV_OFF_RSC + rr * NV_RSC_PITCH + 4 * w;
+    if (4 * w + 4 <= b_end && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+      stg32(dst, lds32(src));
+    } else {
+      for (int bb = 0; bb < 4 && 4 * w + bb < b_end; ++bb) stg8(dst + bb, ld_shared_u8(src + bb));
     }
   }
 }
@@ -473,15 +488,24 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
             bulk_commit();
           }
         } else {
-          // thread tid writes row tid of the band, slots rq_first..slot4
-          const int row = band * NV_BAND + tid;
-          if (row < a.M) {
-            const int srow = (tid & 7) * 32 + (tid >> 3);
-            uint8_t* dst = a.q_row + static_cast<size_t>(row) * (a.K / 2) + kbyte0;
-            for (int sl = rq_first; sl <= slot4; ++sl) {
-              const int scol0 = (tk - slot4 + sl) * NV_STEP_K;   // first column of slot sl
-              for (int q4 = 0; q4 < 8 && scol0 + 8 * q4 < a.K; ++q4)
-                stg32(dst + sl * 32 + 4 * q4, lds32(sbase + NV_OFF_QR + swz128(srow, sl * 32 + 4 * q4)));
+          // A partial group (range or band edge): slots rq_first..slot4 of
+          // every row, each slot's 32 bytes written by two neighbouring
+          // threads in one instruction (16 bytes each), so that it leaves as
+          // one whole sector.  K is a multiple of 32, so a 16-byte half
+          // (32 columns) is either wholly inside the matrix or wholly out.
+          // (One 4-byte store per thread and word instead: 90.4 -> 80.5 us
+          // for the 16384 x 8192 cast, measured on GB300.)
+          const int nsl = slot4 + 1 - rq_first;
+          for (int it = tid; it < NV_BAND * nsl * 2; it += NV_WARPS * 32) {
+            const int rr = it / (2 * nsl);
+            const int rem = it - rr * 2 * nsl;
+            const int sl = rq_first + (rem >> 1), half = rem & 1;
+            const int row = band * NV_BAND + rr;
+            if (row < a.M && (tk - slot4 + sl) * NV_STEP_K + 32 * half < a.K) {
+              const int srow = (rr & 7) * 32 + (rr >> 3);
+              const uint4 v = lds128(sbase + NV_OFF_QR + swz128(srow, sl * 32 + 16 * half));
+              stg128(a.q_row + static_cast<size_t>(row) * (a.K / 2) + kbyte0 + sl * 32 + 16 * half,
+                     v.x, v.y, v.z, v.w);
             }
           }
         }
