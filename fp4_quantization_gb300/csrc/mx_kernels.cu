@@ -60,8 +60,10 @@
 // them apart.
 #if MXQ_TILED_SCALES
 #define MX_KERNEL mx_quantize_tiled_kernel
+#define MX_TILE_KERNEL mx_cast_tile_tiled_kernel
 #else
 #define MX_KERNEL mx_quantize_kernel
+#define MX_TILE_KERNEL mx_cast_tile_kernel
 #endif
 // L2 policies (tuning builds): input copies 1 evict-first, 2 evict-last,
 // 3 evict-normal; colwise code stores 0 none, 1 evict-first, 2 evict-last,
@@ -829,18 +831,35 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
           const int kb0 = (tk - slot) * 4;   // first k-block of the group
           // Two 16-byte halves: every row start must be 16-byte aligned.
           const bool full = rsc_first == 0 && slot == 7 && ((nkb | (obase >> 5)) & 15) == 0;
-          for (int it = tid; it < 2 * BAND; it += THREADS) {
-            const int rr = it >> 1, half = it & 1;
-            const int row = band * BAND + rr;
-            if (row >= a.M) continue;
-            uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + (obase >> 5) + kb0;
-            const uint32_t src = sbase + L::OFF_RSC + ((t * GROUP + pos.bi) * BAND + rr) * 32;
-            if (full) {
+          if (full) {
+            for (int it = tid; it < 2 * BAND; it += THREADS) {
+              const int rr = it >> 1, half = it & 1;
+              const int row = band * BAND + rr;
+              if (row >= a.M) continue;
+              uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + (obase >> 5) + kb0;
+              const uint32_t src = sbase + L::OFF_RSC + ((t * GROUP + pos.bi) * BAND + rr) * 32;
               const uint4 v = lds128(src + 16 * half);
               stg128(dst + 16 * half, v.x, v.y, v.z, v.w);
-            } else if (half == 0) {
-              const int b_end = min((slot + 1) * 4, (a.kin >> 5) - kb0);
-              copy_run_to_global(dst + rsc_first * 4, src + rsc_first * 4, b_end - rsc_first * 4);
+            }
+          } else {
+            // A partial group: eight neighbouring threads per row, thread w
+            // writing the 4 bytes of step slot w when the group has them,
+            // so that the row's run leaves as one request (a step past the
+            // last valid column has fewer bytes).
+            const int b_end = (a.kin >> 5) - kb0;   // valid scale bytes from kb0 on
+            for (int it = tid; it < 8 * BAND; it += THREADS) {
+              const int rr = it >> 3, w = it & 7;
+              const int row = band * BAND + rr;
+              if (row >= a.M || w < rsc_first || w > slot || 4 * w >= b_end) continue;
+              uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + (obase >> 5) + kb0 + 4 * w;
+              const uint32_t src =
+                  sbase + L::OFF_RSC + ((t * GROUP + pos.bi) * BAND + rr) * 32 + 4 * w;
+              if (4 * w + 4 <= b_end && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                stg32(dst, lds32(src));
+              } else {
+                for (int bb = 0; bb < 4 && 4 * w + bb < b_end; ++bb)
+                  stg8(dst + bb, ld_shared_u8(src + bb));
+              }
             }
           }
         }
@@ -869,6 +888,268 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
   }
   // The staged codes must have left shared memory before the CTA exits.
   if (tid == 0) bulk_wait_all();
+}
+
+// ---------------------------------------------------------------------------
+// The plain cast as one CTA per 128 x 128 tile (no activation, no dbias)
+// ---------------------------------------------------------------------------
+//
+// A persistent grid walks 152 separate address ranges at once, and on GB300
+// HBM that costs bandwidth: a copy kernel of the same bytes measured about
+// 12% slower persistent (one CTA per SM, contiguous ranges) than as short
+// CTAs that the block scheduler hands out in address order, which keeps all
+// SMs inside one narrow window of memory.  The plain cast therefore runs as
+// one CTA of 4 warps per 128-row x 128-column tile, tiles numbered along K
+// inside a band: the tile arrives by one TMA copy, the 4 warps take its rows
+// in two 64-row passes (the lane layout and the arithmetic of
+// mx_quantize_kernel), and four CTAs share an SM (at most 128 registers a
+// thread), so one CTA's copy overlaps the others' work.  Rowwise codes leave
+// by streaming stores from registers, colwise codes by one bulk tensor store
+// of the staged tile, scale bytes as one 4-byte run per row and column (or
+// one 512-byte tile each in the tiled layout).
+struct MxTileLayout {
+  static constexpr int WARPS = 4;
+  static constexpr int ROWS = 128;                           // rows of a tile
+  static constexpr int OFF_TILE = 0;                         // [128 rows][256 B] bf16
+  static constexpr int OFF_QCOL = ROWS * MX_TILE_K * 2;      // [k % 8][k / 8][128 m], 16 KiB
+  static constexpr int OFF_RSC = OFF_QCOL + ROWS * MX_TILE_K;   // [128 rows][4 blocks]
+  static constexpr int OFF_CSC = OFF_RSC + ROWS * 4;            // [128 columns][4 blocks]
+  static constexpr int OFF_XCH = OFF_CSC + MX_TILE_K * 4;       // [2 passes][4 warps][16][16 B]
+  static constexpr int BYTES = OFF_XCH + 2 * WARPS * 16 * 16;
+  static constexpr int DYNAMIC = BYTES + 1024;               // + alignment pad
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(MxTileLayout::WARPS * 32, 4)
+MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
+               const __grid_constant__ CUtensorMap tmap_qcol, const MxArgs a) {
+  using L = MxTileLayout;
+  constexpr bool ROW = (MODE & MX_ROW) != 0;
+  constexpr bool COL = (MODE & MX_COL) != 0;
+  constexpr int THREADS = L::WARPS * 32;
+  constexpr int ROW_PITCH = MX_TILE_K * 2;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar;
+
+  uint8_t* smem = align_up_shared<1024>(smem_raw);
+  const uint32_t sbase = smem_addr(smem);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int h = lane >> 4;
+  const int c = lane & 15;
+  const uint32_t bar = smem_addr(&full_bar);
+  const int band = static_cast<int>(blockIdx.x) / a.tiles_k;
+  const int tk = static_cast<int>(blockIdx.x) - band * a.tiles_k;
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, L::ROWS * ROW_PITCH);
+#if MXQ_LOAD_POLICY == 1
+    tma_load_2d_hint(sbase + L::OFF_TILE, &tmap_x, tk * MX_TILE_K, band * L::ROWS, bar,
+                     l2_policy_evict_first());
+#else
+    tma_load_2d(sbase + L::OFF_TILE, &tmap_x, tk * MX_TILE_K, band * L::ROWS, bar);
+#endif
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(bar, 0, a.timeout_ns);
+
+  const uint32_t ceil_bf16 = a.scale_ceil ? 0x001F001Fu : 0u;
+  const int col0 = tk * MX_TILE_K + c * 8;      // first column of this lane
+  const bool col_ok = col0 < a.kin;
+
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int vw = 4 * pass + warp;             // 16-row slice of the tile, 0..7
+    const uint32_t my_row0 = sbase + L::OFF_TILE + (16 * vw + 8 * h) * ROW_PITCH + c * 16;
+    uint32_t xr[8][4];
+    uint32_t ce[4] = {0u, 0u, 0u, 0u};
+    uint32_t re[4] = {0u, 0u, 0u, 0u};
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = lds128(my_row0 + i * ROW_PITCH);
+        xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
+      }
+      uint32_t cm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        uint32_t tt[2];
+#pragma unroll
+        for (int di = 0; di < 2; ++di) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], xr[i + di][p]);
+          tt[di] = absmax_bf16x2(absmax_bf16x2(xr[i + di][0], xr[i + di][1]),
+                                 absmax_bf16x2(xr[i + di][2], xr[i + di][3]));
+        }
+        re[i / 2] = bf16_scale_exponents(
+            absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632)), ceil_bf16);
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p) ce[p] = bf16_scale_exponents(cm[p], ceil_bf16);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xr[i][0] = xr[i][1] = xr[i][2] = xr[i][3] = 0u;
+    }
+    // Column maxima over the warp's 16 rows, published for the partner warp
+    // (the other 16 rows of the same 32-row block); one exchange buffer per
+    // pass, so pass 1 never overwrites what the partner still reads.
+#pragma unroll
+    for (int p = 0; p < 4; ++p) ce[p] = vmax_u16x2(ce[p], __shfl_xor_sync(0xFFFFFFFFu, ce[p], 16));
+    const uint32_t xch = sbase + L::OFF_XCH + ((pass * L::WARPS + warp) * 16 + c) * 16;
+    if (COL && h == 0) sts128(xch, ce[0], ce[1], ce[2], ce[3]);
+    if (pass == 0) {
+      if (__syncthreads_or(!ok)) {
+        // The copy never landed: record it, let it finish (bounded) and stop.
+        if (tid == 0) {
+          if (a.dev_err) atomicOr(a.dev_err, 1u);
+          mbar_wait_bounded(bar, 0, a.timeout_ns);
+        }
+        return;
+      }
+    } else {
+      bar_sync_cta(THREADS);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 1));
+      re[q] = vmax_u16x2(re[q], __shfl_xor_sync(0xFFFFFFFFu, re[q], 2));
+    }
+    if constexpr (COL) {
+      const uint4 other =
+          lds128(sbase + L::OFF_XCH + ((pass * L::WARPS + (warp ^ 1)) * 16 + c) * 16);
+      ce[0] = vmax_u16x2(ce[0], other.x);
+      ce[1] = vmax_u16x2(ce[1], other.y);
+      ce[2] = vmax_u16x2(ce[2], other.z);
+      ce[3] = vmax_u16x2(ce[3], other.w);
+    }
+    const int rl = 16 * vw + 8 * h;                 // first tile row of this lane
+    const int row0 = band * L::ROWS + rl;
+    const bool row_ok = row0 < a.M;
+
+    if constexpr (ROW) {
+      uint32_t rc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) rc[q] = e8m0_pair(re[q]);
+      uint8_t* qrow = a.q_row + static_cast<size_t>(row0) * a.K + col0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float inv = inv_scale_from_e8m0(half16(rc[i >> 1], i & 1));
+        const float2 iv = make_float2(inv, inv);
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 v = mul_f32x2(make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p])), iv);
+          w[p] = cvt_e4m3x2(v.x, v.y);
+        }
+        if (col_ok && row_ok)
+          stg64_cs(qrow + static_cast<size_t>(i) * a.K, w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+      }
+      // Lane (h, c) holds block c / 4 of its 8 rows; it stages rows r and
+      // r + 4 (r = c & 3) into [128 rows][4 blocks].
+      const int r = c & 3, b = c >> 2;
+      const int sh = 16 * (r & 1);
+      sts8(sbase + L::OFF_RSC + (rl + r) * 4 + b, ((r >> 1 ? rc[1] : rc[0]) >> sh) & 0xFFu);
+      sts8(sbase + L::OFF_RSC + (rl + r + 4) * 4 + b, ((r >> 1 ? rc[3] : rc[2]) >> sh) & 0xFFu);
+    }
+
+    if constexpr (COL) {
+      uint32_t cc[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) cc[p] = e8m0_pair(ce[p]);
+      // Staging [k % 8][k / 8][128 m] with the 128-byte swizzle: the lane's
+      // 8 rows are the h-th 8-byte half of chunk vw of each k row.
+      const uint32_t qs = sbase + L::OFF_QCOL + c * 128 + ((vw ^ (c & 7)) << 4) + 8 * h;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 iv = make_float2(inv_scale_from_e8m0(half16(cc[p], 0)),
+                                      inv_scale_from_e8m0(half16(cc[p], 1)));
+        uint32_t we[4], wo[4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const float2 r0 = mul_f32x2(make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p])), iv);
+          const float2 r1 =
+              mul_f32x2(make_float2(bf16_lo(xr[i + 1][p]), bf16_hi(xr[i + 1][p])), iv);
+          we[i / 2] = cvt_e4m3x2(r0.x, r1.x);
+          wo[i / 2] = cvt_e4m3x2(r0.y, r1.y);
+        }
+        sts64(qs + (2 * p) * 2048, we[0] | (we[1] << 16), we[2] | (we[3] << 16));
+        sts64(qs + (2 * p + 1) * 2048, wo[0] | (wo[1] << 16), wo[2] | (wo[3] << 16));
+      }
+      // Scale bytes of block vw / 2 of the tile: the even warp of the pair
+      // writes them, [128 columns][4 blocks].
+      if ((vw & 1) == 0) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint32_t pair = h ? cc[2 + (jj >> 1)] : cc[jj >> 1];
+          sts8(sbase + L::OFF_CSC + (c * 8 + 4 * h + jj) * 4 + (vw >> 1),
+               (pair >> (16 * (jj & 1))) & 0xFFu);
+        }
+      }
+    }
+  }
+
+  // ---- the tile's staging is complete: bulk store and scale runs --------
+  fence_proxy_async_smem();
+  bar_sync_cta(THREADS);
+  if (COL && tid == 0) {
+    tma_store_3d(&tmap_qcol, sbase + L::OFF_QCOL, band * L::ROWS, tk * (MX_TILE_K / 8), 0);
+    bulk_commit();
+  }
+  const int nmb = a.M / 32;    // colwise scale bytes per column
+  const int nkb = a.K / 32;    // rowwise scale bytes per row
+  if constexpr (MXQ_TILED_SCALES) {
+    // One 512-byte tile each: entry (r, c) at (r % 32) * 16 + (r / 32) * 4 + c;
+    // lane L writes rows (columns) L, L + 32, L + 64, L + 96.
+    if (ROW && warp == 0) {
+      const int tiles_kb = (nkb + 3) / 4;
+      const uint32_t src = sbase + L::OFF_RSC + lane * 4;
+      stg128(a.s_row + (static_cast<size_t>(band) * tiles_kb + tk) * 512 + 16 * lane, lds32(src),
+             lds32(src + 32 * 4), lds32(src + 64 * 4), lds32(src + 96 * 4));
+    }
+    if (COL && warp == 1) {
+      const int tiles_mb = (nmb + 3) / 4;
+      const uint32_t src = sbase + L::OFF_CSC + lane * 4;
+      stg128(a.s_col + (static_cast<size_t>(tk) * tiles_mb + band) * 512 + 16 * lane, lds32(src),
+             lds32(src + 32 * 4), lds32(src + 64 * 4), lds32(src + 96 * 4));
+    }
+  } else {
+    if (ROW) {
+      // row tid: blocks 4 tk .. 4 tk + 3, one 4-byte run when aligned
+      const int row = band * L::ROWS + tid;
+      const int nb = min(4, (a.kin >> 5) - 4 * tk);
+      if (row < a.M && nb > 0) {
+        uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + 4 * tk;
+        const uint32_t src = sbase + L::OFF_RSC + tid * 4;
+        if (nb == 4 && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+          stg32(dst, lds32(src));
+        } else {
+          for (int bb = 0; bb < nb; ++bb) stg8(dst + bb, ld_shared_u8(src + bb));
+        }
+      }
+    }
+    if (COL) {
+      // column tid: blocks 4 band .. 4 band + 3 (fewer in the last band).
+      // Evict-last: a run is part of a 32-byte sector that neighbouring
+      // tiles complete, kept in L2 until the sector is whole.
+      const int k = tk * MX_TILE_K + tid;
+      const int nb = min(4, nmb - 4 * band);
+      if (k < a.kin) {
+        uint8_t* dst = a.s_col + static_cast<size_t>(k) * a.scol_ld + 4 * band;
+        const uint32_t src = sbase + L::OFF_CSC + tid * 4;
+        if (nb == 4 && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+          stg32_hint(dst, lds32(src), l2_policy_evict_last());
+        } else {
+          for (int bb = 0; bb < nb; ++bb) stg8(dst + bb, ld_shared_u8(src + bb));
+        }
+      }
+    }
+  }
+  // The staged codes must have left shared memory before the CTA exits.
+  if (COL && tid == 0) bulk_wait_read<0>();
 }
 
 // dbias[k] = sum over bands of the band sums.  A block takes 64 columns with
@@ -1034,9 +1315,42 @@ struct MxConfig<ACT_DSWIGLU> : MxConfigDGated {};
 template <>
 struct MxConfig<ACT_DGEGLU> : MxConfigDGated {};
 
+// The plain cast (no activation, no dbias) as one CTA per tile (see
+// MX_TILE_KERNEL); MXQ_PLAIN_PERSISTENT=1 builds keep the persistent kernel
+// for it instead (tuning comparisons).
+#ifndef MXQ_PLAIN_PERSISTENT
+#define MXQ_PLAIN_PERSISTENT 0
+#endif
+
+template <int MODE>
+cudaError_t launch_tile_variant(const MxMaps& maps, const MxArgs& a, cudaStream_t stream) {
+  using L = MxTileLayout;
+  static_assert(4 * (L::DYNAMIC + 1024) <= 228 * 1024, "four CTAs per SM must fit");
+  auto kernel = MX_TILE_KERNEL<MODE>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (configured_device != dev) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYNAMIC);
+    if (err != cudaSuccess) return err;
+    configured_device = dev;
+  }
+  const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
+  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  kernel<<<static_cast<unsigned>(tiles), L::WARPS * 32, L::DYNAMIC, stream>>>(maps.x, maps.q_col,
+                                                                             a);
+  return cudaGetLastError();
+}
+
 template <int MODE, bool DBIAS, int ACT>
 cudaError_t launch_variant(const MxMaps& maps, const MxArgs& a, int num_sms,
                            cudaStream_t stream) {
+  if constexpr (!DBIAS && ACT == ACT_NONE && !MXQ_PLAIN_PERSISTENT) {
+    static_assert(16 * MxConfig<ACT_NONE>::WARPS == MxTileLayout::ROWS,
+                  "the tile kernel takes the plain cast's bands");
+    return launch_tile_variant<MODE>(maps, a, stream);
+  }
   constexpr int WARPS = MxConfig<ACT>::WARPS;
   constexpr bool PLAIN_DBIAS = DBIAS && ACT == ACT_NONE;   // its own ring / residency
   constexpr int STAGES = PLAIN_DBIAS ? MXQ_DBIAS_STAGES : MxConfig<ACT>::STAGES;

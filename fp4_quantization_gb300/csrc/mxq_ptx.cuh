@@ -122,24 +122,6 @@ __device__ __forceinline__ void stg8(void* p, uint32_t a) {
   asm volatile("st.global.u8 [%0], %1;" :: "l"(p), "r"(a) : "memory");
 }
 
-// Copies n bytes from shared memory (src) to global memory (dst) with the
-// widest stores the alignment of dst allows: single bytes up to a 4-byte
-// boundary, then 4-byte words, then the tail.  For short, unaligned runs
-// (scale bytes at ragged shapes); aligned full runs use vector stores.
-__device__ __forceinline__ void copy_run_to_global(uint8_t* dst, uint32_t src, int n) {
-  int i = 0;
-  while (i < n && (reinterpret_cast<uintptr_t>(dst + i) & 3u)) {
-    stg8(dst + i, ld_shared_u8(src + i));
-    ++i;
-  }
-  for (; i + 4 <= n; i += 4) {
-    const uint32_t w = ld_shared_u8(src + i) | (ld_shared_u8(src + i + 1) << 8) |
-                       (ld_shared_u8(src + i + 2) << 16) | (ld_shared_u8(src + i + 3) << 24);
-    stg32(dst + i, w);
-  }
-  for (; i < n; ++i) stg8(dst + i, ld_shared_u8(src + i));
-}
-
 // ---------------------------------------------------------------------------
 // mbarrier + TMA
 // ---------------------------------------------------------------------------
