@@ -384,16 +384,23 @@ def rows_measurements(mxq, device, steps, warmup, world, stream, peak, only=None
 
 
 def copy_ceiling(device, steps, stream, elems=256 * 2 ** 20):
-    """torch's device-to-device copy of `elems` bf16 values (read + write
-    bytes), timed with events: median and best over `steps` calls."""
+    """What plain copies of `elems` bf16 values (512 MiB in, 512 MiB out, close
+    to the headline cast's 1.09 GB) reach on this GPU, timed with events
+    (median and best over `steps` calls): torch's device-to-device copy (a
+    memcpy, which ncu cannot capture) and torch's elementwise kernel on the
+    same buffers (negation: one read and one write per element, a kernel ncu
+    captures in the same units as the cast)."""
     a = torch.empty(elems, dtype=torch.bfloat16, device=device).normal_()
     b = torch.empty_like(a)
-    _, per_call, _ = time_device(lambda: b.copy_(a), max(3, steps), 3, 1, stream)
     nbytes = 2 * a.numel() * a.element_size()
-    med = statistics.median(per_call)
-    return {"bytes_per_call": nbytes, "us_per_call": round(med * 1e3, 2),
-            "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 1),
-            "best_GB_per_s": round(nbytes / (min(per_call) * 1e-3) / 1e9, 1)}
+    out = {"bytes_per_call": nbytes}
+    for name, fn in (("memcpy", lambda: b.copy_(a)), ("elementwise_neg", lambda: torch.neg(a, out=b))):
+        _, per_call, _ = time_device(fn, max(3, steps), 3, 1, stream)
+        med = statistics.median(per_call)
+        out[name] = {"us_per_call": round(med * 1e3, 2),
+                     "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 1),
+                     "best_GB_per_s": round(nbytes / (min(per_call) * 1e-3) / 1e9, 1)}
+    return out
 
 
 def cold_l2_measure(fn, steps, stream, device, flush_bytes=512 * 2 ** 20):
@@ -537,7 +544,7 @@ def gpu_arm(args):
         "data": "synthetic: N(0,1) bf16, Philox seed 5",
         "config": {"workload": f"mxfp8_rowwise_colwise_{M}x{K}", "M": M, "K": K, "block": 32,
                    "directions": "rowwise+colwise", "parallelism": f"replicas x{world}",
-                   "l2": "input 512 MiB > 129 MiB L2: no flush between steps"},
+                   "l2": f"input {M * K * 2 // 2**20} MiB > 129 MiB L2: no flush between steps"},
         "clocks": clocks.summary(),
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
