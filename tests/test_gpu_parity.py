@@ -27,6 +27,11 @@ def _rowcol_cases():
         ("tall_thin", synth.rowcol(M=640, K=32, seed=32), 0),
         ("wide_short", synth.dim1(M=32, K=1056, seed=33), 0),
         ("many_tiles", synth.dbias(M=512, K=1024, seed=34), 0),
+        # colwise scale rows of 5 bytes (M / 32 = 5: unaligned 4-byte runs)
+        # and a last band of 32 rows
+        ("odd_scale_rows", synth.rowcol(M=160, K=288, seed=35), 0),
+        # 33 bands, the last one 32 rows, over 2 tiles along K
+        ("ragged_last_band", synth.rowcol(M=4128, K=160, seed=36), 0),
     ]
 
 
