@@ -1,16 +1,23 @@
 // mx_kernels.cu -- MXFP8 quantization kernels for sm_103a.
 //
-// One kernel template covers the MXFP8 paths of TE PR #3291 "Fix pointer
-// arithmatic to generate correct LDS/STS instructions" (results tables
-// "MXFP8 generic quantize kernel": plain / dbias / gelu; "MXFP8 specialized
-// cast-only kernel (bidimensional)": plain row / both; "MXFP8 gated (swiglu /
-// geglu) kernel": swiglu) and the colwise "dim1" cast of torchao PR #12
-// "Multiply with inverse scale in loop instead of dividing".
+// Two kernels cover the MXFP8 paths of TE PR #3291 "Fix pointer arithmatic
+// to generate correct LDS/STS instructions" (results tables "MXFP8 generic
+// quantize kernel": plain / dbias / gelu; "MXFP8 specialized cast-only
+// kernel (bidimensional)": plain row / both; "MXFP8 gated (swiglu / geglu)
+// kernel": swiglu) and the colwise "dim1" cast of torchao PR #12 "Multiply
+// with inverse scale in loop instead of dividing":
+//  * the plain cast runs mx_cast_tile_kernel, one short CTA per 128 x 128
+//    tile dispatched in address order (see its comment: a persistent grid
+//    reads and writes HBM more slowly on GB300);
+//  * the fused paths (dbias, GELU, SwiGLU / GeGLU, the backward fusions)
+//    run the persistent mx_quantize_kernel described here, whose TMA ring
+//    overlaps the next tile's copy with the arithmetic they need.
+// Both use the same lane layout and arithmetic.
 //
 // The path is bound by HBM traffic, and on GB300 the write side costs by
 // the number of L2 write requests rather than by bytes: a 1-byte store costs
-// as much as a 32-byte one.  The kernel is laid out so every output leaves
-// in whole sectors or lines:
+// as much as a 32-byte one.  The persistent kernel is laid out so every
+// output leaves in whole sectors or lines:
 //  * One CTA of WARPS warps per SM (persistent) walks a contiguous range of
 //    "steps"; a step is a band of BAND = 16 * WARPS rows x 128 columns,
 //    loaded by one TMA box into a ring of STAGES slots (one mbarrier per
