@@ -107,25 +107,28 @@ mxq_status encode_mx_qrow_map(CUtensorMap* map, uint8_t* base, int64_t M, int64_
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// NVFP4 code maps: rowwise [M][K/2] seen as [m % 8][m / 8][k / 2] (box
-// 128 B x band / 8 x 8) and transposed [K][M/2] seen as [k % 8][k / 8][m / 2]
-// (box 128 B x step / 8 x 8), both with the 128-byte swizzle.
+// NVFP4 code maps: rowwise [M][K/2] seen as [m % 8][m / 8][k / 2] and
+// transposed [K][M/2] seen as [k % 8][k / 8][m / 2].  The persistent kernel
+// stores boxes of 128 B x rows / 8 (cols / 8) x 8 with the 128-byte swizzle,
+// the tile kernel boxes of 64 B x 16 x 8 with the 64-byte swizzle.
 mxq_status encode_nv_code_maps(mxq::NvMaps* maps, uint32_t flags, int64_t M, int64_t K,
-                               uint8_t* q_row, uint8_t* q_t) {
+                               uint8_t* q_row, uint8_t* q_t, const mxq::NvShape& shp) {
+  const cuuint32_t inner = shp.tiles ? 64 : 128;
+  const CUtensorMapSwizzle swz = shp.tiles ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   if (flags & MXQ_ROWWISE) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M / 8), 8};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * K), static_cast<cuuint64_t>(K / 2)};
-    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(mxq::nv_band_rows() / 8), 8};
+    const cuuint32_t box[3] = {inner, static_cast<cuuint32_t>(shp.rows / 8), 8};
     mxq_status st = encode_map(&maps->q_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q_row, dims,
-                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+                               strides, box, swz);
     if (st != MXQ_OK) return st;
   }
   if (flags & MXQ_COLWISE) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(M / 2), static_cast<cuuint64_t>(K / 8), 8};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * M), static_cast<cuuint64_t>(M / 2)};
-    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(mxq::nv_step_cols() / 8), 8};
+    const cuuint32_t box[3] = {inner, static_cast<cuuint32_t>(shp.cols / 8), 8};
     mxq_status st = encode_map(&maps->q_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q_t, dims, strides,
-                               box, CU_TENSOR_MAP_SWIZZLE_128B);
+                               box, swz);
     if (st != MXQ_OK) return st;
   }
   return MXQ_OK;
@@ -522,13 +525,13 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
     if (st != MXQ_OK) return st;
     amax = ws_amax;
   }
-  const int band = mxq::nv_band_rows();
-  const int step = mxq::nv_step_cols();
+  const bool two_d = (flags & MXQ_NVFP4_2D) != 0;
+  const mxq::NvShape shp = mxq::nv_shape(two_d);
   mxq::NvArgs a{};
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
-  a.tiles_m = static_cast<int>((M + band - 1) / band);
-  a.tiles_k = static_cast<int>((K + step - 1) / step);
+  a.tiles_m = static_cast<int>((M + shp.rows - 1) / shp.rows);
+  a.tiles_k = static_cast<int>((K + shp.cols - 1) / shp.cols);
   a.amax = amax;
   a.global_scale = global_scale;
   a.q_row = q_row;
@@ -539,10 +542,9 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   mxq::NvMaps maps{};
   const int mode = direction_mode(flags);
-  const bool two_d = (flags & MXQ_NVFP4_2D) != 0;
-  st = encode_bf16_map(&maps.x, x, M, K, ldx, step, band);
+  st = encode_bf16_map(&maps.x, x, M, K, ldx, shp.cols, shp.rows);
   if (st != MXQ_OK) return st;
-  st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t);
+  st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t, shp);
   if (st != MXQ_OK) return st;
   return from_cuda(mxq::launch_nvfp4(maps, a, mode, two_d, sms, amax_in == nullptr, stream));
 }

@@ -523,6 +523,336 @@ nvfp4_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x,
   if (tid == 0) bulk_wait_all();
 }
 
+// ---------------------------------------------------------------------------
+// One CTA per 128 x 128 tile
+// ---------------------------------------------------------------------------
+//
+// Short CTAs handed out in address order read and write HBM faster on GB300
+// than a persistent grid, but a short CTA cannot afford the persistent
+// kernel's scale table (one entry per possible block amax).  This kernel
+// keeps only a 128-entry table of 1/d by scale code and decides each code
+// from one multiply (NvFastScale); the rare blocks the multiply cannot decide
+// take the recipe's own division sequence.  One CTA of 4 warps takes a
+// 128 x 128 tile (one TMA copy) in two 64-column passes with the persistent
+// kernel's lane layout (lane (h, c) of warp w: rows 32w + 8h + 0..7,
+// columns 8c..8c+7 of the pass).  Codes are staged per tile and leave by one
+// 3-D bulk tensor store per direction (64-byte rows, 64-byte swizzle); scale
+// bytes as one 8-byte run per row and per column, evict-last (a quarter of a
+// 32-byte sector that the neighbouring tiles complete).  Four CTAs share an
+// SM.
+constexpr int NT_WARPS = 4;
+constexpr int NT_ROWS = 128;
+constexpr int NT_COLS = 128;
+constexpr int NT_TILE_BYTES = NT_ROWS * NT_COLS * 2;            // 32 KiB of bf16
+constexpr int NT_OFF_QR = NT_TILE_BYTES;                         // [m % 8][m / 8][64 B]
+constexpr int NT_OFF_QT = NT_OFF_QR + NT_ROWS * NT_COLS / 2;     // [k % 8][k / 8][64 B]
+constexpr int NT_OFF_RSC = NT_OFF_QT + NT_COLS * NT_ROWS / 2;    // [128 rows][8 blocks]
+constexpr int NT_OFF_TSC = NT_OFF_RSC + NT_ROWS * 8;             // [8 blocks][128 columns]
+constexpr int NT_OFF_INV = NT_OFF_TSC + NT_COLS * 8;             // [128 codes] fp32 1/d
+constexpr int NT_SMEM = NT_OFF_INV + 128 * 4 + 1024;             // + alignment pad
+static_assert(4 * (NT_SMEM + 1024) <= 228 * 1024, "four CTAs per SM");
+
+// Byte offset inside a [rows][64 B] staging block whose TMA map uses the
+// 64-byte swizzle: the 16-byte chunk index is xor-ed with (row / 2) % 4.
+__device__ __forceinline__ uint32_t swz64(int row, int byte) {
+  return row * 64 + ((((byte >> 4) ^ ((row >> 1) & 3)) << 4) | (byte & 15));
+}
+
+// Scale codes without a per-amax table.  q = b * K with K = 1 / (6 G) is
+// within a few units in the last place of the recipe's (b / 6) / G (two
+// roundings each side); the codes of the fp32 values 16 units below and
+// above q bound the recipe's code, so when they agree it is that code.  They
+// disagree only within 16 units of an E4M3 rounding boundary -- in practice
+// exact ties, e.g. G a power of two -- and those blocks, like every block
+// when G is below 2^-100 (where b / 6 may round as a subnormal), take the
+// recipe's division sequence.  1/d depends on the code alone: a 128-entry
+// table built once per CTA with the recipe's operations.
+struct NvFastScale {
+  float K;            // 1 / (6 G), rounded twice
+  float G;
+  bool fast;          // 2^-100 <= G <= FLT_MAX
+  uint32_t inv_tab;   // shared address of the [128] table of 1/d by code
+};
+
+__device__ __forceinline__ uint32_t nv_code_try(uint32_t mag, float K, uint32_t& miss) {
+  const int q = __float_as_int(__fmul_rn(__uint_as_float(mag << 16), K));
+  const uint32_t pair = cvt_e4m3x2(__int_as_float(max(q - 16, 0)),
+                                   __int_as_float(min(q + 16, 0x7F7FFFFF)));
+  miss |= pair ^ (pair >> 8);   // low byte nonzero: the two codes differ
+  return pair & 0xFFu;
+}
+
+// The recipe's code for block amax bits `mag`: E4M3((b / 6) / G).
+__device__ __forceinline__ uint32_t nv_code_exact(uint32_t mag, float G) {
+  if (G == 0.0f) return 0u;
+  return cvt_e4m3x2(__fdiv_rn(__fdiv_rn(__uint_as_float(mag << 16), 6.0f), G), 0.0f) & 0xFFu;
+}
+
+// A shared load the compiler may schedule freely: the table it reads is
+// written before the CTA's first barrier and never again.
+__device__ __forceinline__ float lds_table_f32(uint32_t addr) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// Codes and reciprocals of N blocks whose amax bits are the bf16 halves of
+// m[0..N/2) (block i: half i & 1 of m[i / 2]).
+template <int N>
+__device__ __forceinline__ void nv_scales(const uint32_t* m, const NvFastScale& fs,
+                                          uint32_t* code, float* inv) {
+  uint32_t miss = fs.fast ? 0u : 1u;
+#pragma unroll
+  for (int i = 0; i < N; ++i) code[i] = nv_code_try(mag16(m[i >> 1], i & 1), fs.K, miss);
+  if (miss & 0xFFu) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      uint32_t one = fs.fast ? 0u : 1u;
+      nv_code_try(mag16(m[i >> 1], i & 1), fs.K, one);
+      if (one & 0xFFu) code[i] = nv_code_exact(mag16(m[i >> 1], i & 1), fs.G);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) inv[i] = lds_table_f32(fs.inv_tab + 4 * code[i]);
+}
+
+template <int MODE, bool TWO_D>
+__global__ void __launch_bounds__(NT_WARPS * 32, 4)
+nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                  const __grid_constant__ CUtensorMap tmap_qrow,
+                  const __grid_constant__ CUtensorMap tmap_qt, const NvArgs a) {
+  constexpr bool ROW = (MODE & MX_ROW) != 0;
+  constexpr bool COL = (MODE & MX_COL) != 0;
+  constexpr int ROW_PITCH = NT_COLS * 2;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar;
+  uint8_t* smem = align_up_shared<1024>(smem_raw);
+  const uint32_t sbase = smem_addr(smem);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int h = lane >> 3;   // 8-row group 0..3 of the warp's 32 rows
+  const int c = lane & 7;    // 8-column chunk 0..7 of the pass's 64 columns
+  const uint32_t bar = smem_addr(&full_bar);
+  const int band = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.tiles_k));
+  const int tk = static_cast<int>(blockIdx.x) - band * a.tiles_k;
+
+  if (tid == 0) {
+    if (ROW) prefetch_tensormap(&tmap_qrow);
+    if (COL) prefetch_tensormap(&tmap_qt);
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, NT_TILE_BYTES);
+    tma_load_2d(sbase, &tmap_x, tk * NT_COLS, band * NT_ROWS, bar);
+  }
+  // The tensor amax, read while the copy is in flight (after the amax grid
+  // this one may depend on has completed), and the table of 1/d by code
+  // (the recipe's d = value(s) * G, 1/d rounded to nearest).
+  grid_dependency_wait();
+  NvFastScale fs;
+  {
+    const float A = *a.amax;
+    fs.G = __fdiv_rn(A, 2688.0f);
+    fs.K = __frcp_rn(__fmul_rn(6.0f, fs.G));
+    fs.fast = fs.G >= 0x1p-100f && fs.G <= FLT_MAX;
+    fs.inv_tab = sbase + NT_OFF_INV;
+    if (blockIdx.x == 0 && tid == 0) *a.global_scale = fs.G;
+    float inv = 0.0f;
+    if (tid != 0) {
+      const float d = __fmul_rn(e4m3_to_f32(static_cast<uint32_t>(tid)), fs.G);
+      if (d != 0.0f) {
+        inv = __frcp_rn(d);
+        if (isinf(inv)) inv = FLT_MAX;
+      }
+    }
+    sts32(fs.inv_tab + 4 * tid, __float_as_uint(inv));
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(bar, 0, a.timeout_ns);
+  if (__syncthreads_or(!ok)) {
+    // The copy never landed: record it, let it finish (bounded) and stop.
+    if (tid == 0) {
+      if (a.dev_err) atomicOr(a.dev_err, 1u);
+      mbar_wait_bounded(bar, 0, a.timeout_ns);
+    }
+    return;
+  }
+
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    // ---- this lane's 8 x 8 block; magnitude maxima ---------------------------
+    const uint32_t my_row0 = sbase + (32 * warp + 8 * h) * ROW_PITCH + (64 * pass + 8 * c) * 2;
+    uint32_t xr[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = lds128(my_row0 + i * ROW_PITCH);
+      xr[i][0] = v.x; xr[i][1] = v.y; xr[i][2] = v.z; xr[i][3] = v.w;
+    }
+    uint32_t cm[4] = {0u, 0u, 0u, 0u};   // columns 2p / 2p+1 over the lane's 8 rows
+    uint32_t rm[4] = {0u, 0u, 0u, 0u};   // rows 2q / 2q+1 over the lane's 8 columns
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      uint32_t tt[2];
+#pragma unroll
+      for (int di = 0; di < 2; ++di) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) cm[p] = absmax_bf16x2(cm[p], xr[i + di][p]);
+        tt[di] = absmax_bf16x2(absmax_bf16x2(xr[i + di][0], xr[i + di][1]),
+                               absmax_bf16x2(xr[i + di][2], xr[i + di][3]));
+      }
+      rm[i / 2] = absmax_bf16x2(prmt(tt[0], tt[1], 0x5410), prmt(tt[0], tt[1], 0x7632));
+    }
+
+    // 2D: the 16x16 block's amax over the four lanes that hold it, and its
+    // one scale.
+    uint32_t code2d = 0u;
+    float inv2d = 0.0f;
+    if constexpr (TWO_D) {
+      uint32_t m2 = absmax_bf16x2(absmax_bf16x2(rm[0], rm[1]), absmax_bf16x2(rm[2], rm[3]));
+      m2 = absmax_bf16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
+      m2 = absmax_bf16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 8));
+      const uint32_t mm = max(mag16(m2, 0), mag16(m2, 1));
+      nv_scales<1>(&mm, fs, &code2d, &inv2d);
+    }
+
+    float2 xv[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) xv[i][p] = make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p]));
+
+    // ---- rowwise: block scales (split over the c pair), codes, scale bytes --
+    if constexpr (ROW) {
+      const int mine = c & 1;               // this lane gathers the scale bytes of rows 4*mine..
+      uint32_t rcode[4];
+      float rinv[8];
+      if constexpr (TWO_D) {
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) rcode[tq] = code2d;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rinv[i] = inv2d;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          rm[q] = absmax_bf16x2(rm[q], __shfl_xor_sync(0xFFFFFFFFu, rm[q], 1));
+        uint32_t code8[8];
+        nv_scales<8>(rm, fs, code8, rinv);
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) rcode[tq] = mine ? code8[4 + tq] : code8[tq];
+      }
+      // Codes of row i: 8 values -> 4 bytes at byte 32 * pass + 4c of the
+      // row's 64; staging row (m % 8) * 16 + m / 8.
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 iv = make_float2(rinv[i], rinv[i]);
+        const float2 v0 = mul_f32x2(xv[i][0], iv);
+        const float2 v1 = mul_f32x2(xv[i][1], iv);
+        const float2 v2 = mul_f32x2(xv[i][2], iv);
+        const float2 v3 = mul_f32x2(xv[i][3], iv);
+        sts32(sbase + NT_OFF_QR + swz64(16 * i + 4 * warp + h, 32 * pass + 4 * c),
+              cvt_e2m1x8(v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y));
+      }
+      // Scale bytes: the four lanes c = mine, mine + 2, mine + 4, mine + 6
+      // hold blocks 0..3 of the pass for the same four rows; lane b = c / 2
+      // gathers row 4 * mine + b (three shuffles) and stores one word.
+      const int b = c >> 1;
+      uint32_t word = pick4(rcode, b) << (8 * b);
+#pragma unroll
+      for (int k = 1; k < 4; ++k) {
+        const int src_b = (b + k) & 3;
+        const uint32_t got = __shfl_sync(0xFFFFFFFFu, pick4(rcode, (b - k) & 3),
+                                         (lane & ~7) | (2 * src_b + mine));
+        word |= got << (8 * src_b);
+      }
+      sts32(sbase + NT_OFF_RSC + (32 * warp + 8 * h + 4 * mine + b) * 8 + 4 * pass, word);
+    }
+
+    // ---- transposed: block scales (split over the h pair), codes, scales ----
+    if constexpr (COL) {
+      const int mine = h & 1;               // this lane stores the scale bytes of columns 4*mine..
+      uint32_t tcode[4];
+      float tinv[8];
+      if constexpr (TWO_D) {
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) tcode[tq] = code2d;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tinv[j] = inv2d;
+      } else {
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          cm[p] = absmax_bf16x2(cm[p], __shfl_xor_sync(0xFFFFFFFFu, cm[p], 8));
+        uint32_t code8[8];
+        nv_scales<8>(cm, fs, code8, tinv);
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) tcode[tq] = mine ? code8[4 + tq] : code8[tq];
+      }
+      // Codes of column k = 64 * pass + 8c + j: 8 rows -> 4 bytes at byte
+      // 16w + 4h of the column's 64; staging row (k % 8) * 16 + k / 8.
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 iv = make_float2(tinv[2 * p], tinv[2 * p + 1]);
+        float2 r[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[i] = mul_f32x2(xv[i][p], iv);
+        const int srow = 16 * (2 * p) + 8 * pass + c;
+        sts32(sbase + NT_OFF_QT + swz64(srow, 16 * warp + 4 * h),
+              cvt_e2m1x8(r[0].x, r[1].x, r[2].x, r[3].x, r[4].x, r[5].x, r[6].x, r[7].x));
+        sts32(sbase + NT_OFF_QT + swz64(srow + 16, 16 * warp + 4 * h),
+              cvt_e2m1x8(r[0].y, r[1].y, r[2].y, r[3].y, r[4].y, r[5].y, r[6].y, r[7].y));
+      }
+      // Scale bytes [block][column]: the lane's four columns are adjacent.
+      sts32(sbase + NT_OFF_TSC + (2 * warp + (h >> 1)) * NT_COLS + 64 * pass + 8 * c + 4 * mine,
+            tcode[0] | (tcode[1] << 8) | (tcode[2] << 16) | (tcode[3] << 24));
+    }
+  }
+
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    if (ROW) tma_store_3d(&tmap_qrow, sbase + NT_OFF_QR, tk * (NT_COLS / 2), band * (NT_ROWS / 8), 0);
+    if (COL) tma_store_3d(&tmap_qt, sbase + NT_OFF_QT, band * (NT_ROWS / 2), tk * (NT_COLS / 8), 0);
+    bulk_commit();
+  }
+  const uint64_t policy = l2_policy_evict_last();
+  if (ROW) {
+    // row tid: blocks 8 tk .. 8 tk + 7 of s_row [M][K / 16]
+    const int nkb = a.K / 16;
+    const int row = band * NT_ROWS + tid;
+    const int nb = min(8, nkb - 8 * tk);
+    if (row < a.M) {
+      uint8_t* dst = a.s_row + static_cast<size_t>(row) * nkb + 8 * tk;
+      const uint32_t src = sbase + NT_OFF_RSC + tid * 8;
+      if (nb == 8 && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+        const uint2 w = lds64(src);
+        stg64_hint(dst, w.x, w.y, policy);
+      } else {
+        for (int bb = 0; bb < nb; ++bb) stg8(dst + bb, ld_shared_u8(src + bb));
+      }
+    }
+  }
+  if (COL) {
+    // column tid: blocks 8 band .. 8 band + 7 of s_t [K][M / 16]
+    const int nmb = a.M / 16;
+    const int k = tk * NT_COLS + tid;
+    const int nb = min(8, nmb - 8 * band);
+    if (k < a.K) {
+      uint8_t* dst = a.s_t + static_cast<size_t>(k) * nmb + 8 * band;
+      const uint32_t src = sbase + NT_OFF_TSC + tid;
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) w[bb >> 2] |= ld_shared_u8(src + bb * NT_COLS) << (8 * (bb & 3));
+      if (nb == 8 && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+        stg64_hint(dst, w[0], w[1], policy);
+      } else {
+        for (int bb = 0; bb < nb; ++bb) stg8(dst + bb, (w[bb >> 2] >> (8 * (bb & 3))) & 0xFFu);
+      }
+    }
+  }
+  // The staged codes must have left shared memory before the CTA exits.
+  if (tid == 0) bulk_wait_read<0>();
+}
+
 // Largest |x| of a bf16 matrix.  Each block takes whole rows; 16-byte loads;
 // the bf16 magnitude bits are order-preserving, so the maximum is taken on
 // integers and the fp32 bit pattern (bf16 << 16) is folded into *out with
@@ -614,21 +944,72 @@ cudaError_t launch_nv_variant(const NvMaps& maps, const NvArgs& a, int num_sms, 
                           after_amax, stream);
 }
 
+// One launch of the tile kernel: one CTA per 128 x 128 tile, in address
+// order (programmatic dependent of this call's own amax grid, as above).
+template <int MODE, bool TWO_D>
+cudaError_t launch_nv_tile_variant(const NvMaps& maps, const NvArgs& a, bool after_amax,
+                                   cudaStream_t stream) {
+  static int configured_device = -1;
+  auto kernel = nvfp4_tile_kernel<MODE, TWO_D>;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (configured_device != dev) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, NT_SMEM);
+    if (err != cudaSuccess) return err;
+    configured_device = dev;
+  }
+  const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
+  if (tiles < 1 || tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles));
+  cfg.blockDim = dim3(NT_WARPS * 32);
+  cfg.dynamicSmemBytes = NT_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_amax ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, maps.x, maps.q_row, maps.q_t, a);
+}
+
+// Which kernel takes 1D and 2D blocks: the tile kernel (1) or the
+// persistent kernel (0).
+#ifndef MXQ_NV1D_TILES
+#define MXQ_NV1D_TILES 1
+#endif
+#ifndef MXQ_NV2D_TILES
+#define MXQ_NV2D_TILES 1
+#endif
+
 template <bool TWO_D>
 cudaError_t launch_nv_mode(const NvMaps& maps, const NvArgs& a, int mode, int num_sms,
                            bool after_amax, cudaStream_t stream) {
-  switch (mode) {
-    case MX_ROW: return launch_nv_variant<MX_ROW, TWO_D>(maps, a, num_sms, after_amax, stream);
-    case MX_COL: return launch_nv_variant<MX_COL, TWO_D>(maps, a, num_sms, after_amax, stream);
-    default:
-      return launch_nv_variant<MX_ROW | MX_COL, TWO_D>(maps, a, num_sms, after_amax, stream);
+  constexpr bool TILES = TWO_D ? MXQ_NV2D_TILES != 0 : MXQ_NV1D_TILES != 0;
+  if constexpr (TILES) {
+    switch (mode) {
+      case MX_ROW: return launch_nv_tile_variant<MX_ROW, TWO_D>(maps, a, after_amax, stream);
+      case MX_COL: return launch_nv_tile_variant<MX_COL, TWO_D>(maps, a, after_amax, stream);
+      default:
+        return launch_nv_tile_variant<MX_ROW | MX_COL, TWO_D>(maps, a, after_amax, stream);
+    }
+  } else {
+    switch (mode) {
+      case MX_ROW: return launch_nv_variant<MX_ROW, TWO_D>(maps, a, num_sms, after_amax, stream);
+      case MX_COL: return launch_nv_variant<MX_COL, TWO_D>(maps, a, num_sms, after_amax, stream);
+      default:
+        return launch_nv_variant<MX_ROW | MX_COL, TWO_D>(maps, a, num_sms, after_amax, stream);
+    }
   }
 }
 
 }  // namespace
 
-int nv_band_rows() { return NV_BAND; }
-int nv_step_cols() { return NV_STEP_K; }
+NvShape nv_shape(bool two_d) {
+  const bool tiles = two_d ? MXQ_NV2D_TILES != 0 : MXQ_NV1D_TILES != 0;
+  return tiles ? NvShape{true, NT_ROWS, NT_COLS} : NvShape{false, NV_BAND, NV_STEP_K};
+}
 
 cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two_d,
                          int num_sms, bool after_amax, cudaStream_t stream) {

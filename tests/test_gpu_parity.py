@@ -423,6 +423,59 @@ def test_nvfp4_2d_caller_amax_and_wide_range(amax_factor):
         assert_equal_bytes(host(out[key]), ref[key], f"2d amax x{amax_factor} {key}")
 
 
+def _scaled_bits(bits, factor):
+    return synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(bits) * np.float32(factor))
+
+
+def _nvfp4_case(bits, A, flags, what):
+    x = to_device(bits)
+    amax = None if A is None else torch.tensor([np.float32(A)], device="cuda")
+    out = mxq.nvfp4_quantize_transpose(x, flags, amax=amax)
+    ref = oracle.nvfp4_quantize(bits, flags=flags,
+                                **({} if A is None else {"tensor_amax": float(np.float32(A))}))
+    assert host(out["global_scale"])[0] == np.float32(ref["global_scale"]), what
+    for key in ("q_row", "s_row", "q_t", "s_t"):
+        assert_equal_bytes(host(out[key]), ref[key], f"{what} {key}")
+
+
+@pytest.mark.parametrize("two_d", [False, True], ids=["1d", "2d"])
+def test_nvfp4_exact_ties(two_d):
+    """G = 1 (caller amax 2688) and values 6 * (j / 16) * 2^e with j in
+    16..31: for odd j the block's (b / 6) / G is exactly halfway between two
+    E4M3 values, the case a one-multiply estimate of the quotient cannot
+    decide and the division sequence must (ties to even)."""
+    rng = np.random.default_rng(64)
+    M, K = 256, 384
+    j = rng.integers(16, 32, size=(M, K))
+    e = rng.integers(-6, 5, size=(M, K))
+    sign = rng.choice([-1.0, 1.0], size=(M, K))
+    f = (sign * 6.0 * j / 16.0 * np.exp2(e)).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(f)
+    # Most row blocks' amaxes are such ties.
+    b = np.abs(f).reshape(M, K // 16, 16).max(axis=2) / 6.0
+    sig = b / np.exp2(np.floor(np.log2(b)))
+    assert np.mean((sig * 16) % 2 == 1) > 0.3
+    _nvfp4_case(bits, 2688.0, BOTH | (mxq.NVFP4_2D if two_d else 0), "ties")
+
+
+@pytest.mark.parametrize("two_d", [False, True], ids=["1d", "2d"])
+@pytest.mark.parametrize("log2_scale", [-97, -90], ids=["amax_2^-95", "amax_2^-88"])
+def test_nvfp4_tiny_tensor_amax(two_d, log2_scale):
+    """Tensor amaxes near 2^-95 (G below 2^-100: every block takes the
+    division sequence) and 2^-88 (just above), with zero, subnormal and
+    outlier blocks."""
+    bits = _scaled_bits(synth.dbias(M=256, K=384, seed=65), 2.0 ** log2_scale)
+    _nvfp4_case(bits, None, BOTH | (mxq.NVFP4_2D if two_d else 0), f"scale 2^{log2_scale}")
+
+
+@pytest.mark.parametrize("two_d", [False, True], ids=["1d", "2d"])
+def test_nvfp4_caller_amax_far_below_data(two_d):
+    """Data near 2^100 with a caller amax of 2^-60: (b / 6) / G overflows to
+    infinity and every block saturates to code 0x7E."""
+    bits = _scaled_bits(synth.nvfp4(M=128, K=256, seed=66), 2.0 ** 100)
+    _nvfp4_case(bits, 2.0 ** -60, BOTH | (mxq.NVFP4_2D if two_d else 0), "amax 2^-60")
+
+
 def test_sharded_helpers_single_rank_nccl():
     """The sharded helpers through NCCL on a one-rank group (this box has one
     GPU): the collectives pass device tensors and the results equal the
