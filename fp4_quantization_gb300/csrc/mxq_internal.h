@@ -96,6 +96,7 @@ struct NvArgs {
   uint8_t* s_t;
   uint32_t* dev_err;
   uint64_t timeout_ns;
+  int reverse;              // tile kernel: take the tiles last first
 };
 
 // Rows per band (per CTA step) of the MXFP8 kernel for activation `act`.
