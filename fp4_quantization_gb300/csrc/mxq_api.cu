@@ -108,27 +108,24 @@ mxq_status encode_mx_qrow_map(CUtensorMap* map, uint8_t* base, int64_t M, int64_
 }
 
 // NVFP4 code maps: rowwise [M][K/2] seen as [m % 8][m / 8][k / 2] and
-// transposed [K][M/2] seen as [k % 8][k / 8][m / 2].  The persistent kernel
-// stores boxes of 128 B x rows / 8 (cols / 8) x 8 with the 128-byte swizzle,
-// the tile kernel boxes of 64 B x 16 x 8 with the 64-byte swizzle.
+// transposed [K][M/2] seen as [k % 8][k / 8][m / 2]; boxes of one tile's
+// codes (64 bytes x 16 x 8) with the 64-byte swizzle.
 mxq_status encode_nv_code_maps(mxq::NvMaps* maps, uint32_t flags, int64_t M, int64_t K,
-                               uint8_t* q_row, uint8_t* q_t, const mxq::NvShape& shp) {
-  const cuuint32_t inner = shp.tiles ? 64 : 128;
-  const CUtensorMapSwizzle swz = shp.tiles ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+                               uint8_t* q_row, uint8_t* q_t) {
   if (flags & MXQ_ROWWISE) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M / 8), 8};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * K), static_cast<cuuint64_t>(K / 2)};
-    const cuuint32_t box[3] = {inner, static_cast<cuuint32_t>(shp.rows / 8), 8};
+    const cuuint32_t box[3] = {mxq::NV_TILE_COLS / 2, mxq::NV_TILE_ROWS / 8, 8};
     mxq_status st = encode_map(&maps->q_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q_row, dims,
-                               strides, box, swz);
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != MXQ_OK) return st;
   }
   if (flags & MXQ_COLWISE) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(M / 2), static_cast<cuuint64_t>(K / 8), 8};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * M), static_cast<cuuint64_t>(M / 2)};
-    const cuuint32_t box[3] = {inner, static_cast<cuuint32_t>(shp.cols / 8), 8};
+    const cuuint32_t box[3] = {mxq::NV_TILE_ROWS / 2, mxq::NV_TILE_COLS / 8, 8};
     mxq_status st = encode_map(&maps->q_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q_t, dims, strides,
-                               box, swz);
+                               box, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != MXQ_OK) return st;
   }
   return MXQ_OK;
@@ -526,12 +523,11 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
     amax = ws_amax;
   }
   const bool two_d = (flags & MXQ_NVFP4_2D) != 0;
-  const mxq::NvShape shp = mxq::nv_shape(two_d);
   mxq::NvArgs a{};
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
-  a.tiles_m = static_cast<int>((M + shp.rows - 1) / shp.rows);
-  a.tiles_k = static_cast<int>((K + shp.cols - 1) / shp.cols);
+  a.tiles_m = static_cast<int>((M + mxq::NV_TILE_ROWS - 1) / mxq::NV_TILE_ROWS);
+  a.tiles_k = static_cast<int>((K + mxq::NV_TILE_COLS - 1) / mxq::NV_TILE_COLS);
   a.amax = amax;
   a.global_scale = global_scale;
   a.q_row = q_row;
@@ -542,11 +538,11 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   mxq::NvMaps maps{};
   const int mode = direction_mode(flags);
-  st = encode_bf16_map(&maps.x, x, M, K, ldx, shp.cols, shp.rows);
+  st = encode_bf16_map(&maps.x, x, M, K, ldx, mxq::NV_TILE_COLS, mxq::NV_TILE_ROWS);
   if (st != MXQ_OK) return st;
-  st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t, shp);
+  st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t);
   if (st != MXQ_OK) return st;
-  return from_cuda(mxq::launch_nvfp4(maps, a, mode, two_d, sms, amax_in == nullptr, stream));
+  return from_cuda(mxq::launch_nvfp4(maps, a, mode, two_d, amax_in == nullptr, stream));
 }
 
 mxq_status mxq_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* dev_err, mxq_stream_t stream) {

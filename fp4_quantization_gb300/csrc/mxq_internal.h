@@ -65,29 +65,23 @@ struct MxMaps {
   CUtensorMap q_row2;
 };
 
-// TMA descriptors of one NVFP4 call: the bf16 input (box nv_shape().cols
-// columns x .rows rows), the rowwise codes [M][K/2] seen as
-// [m % 8][m / 8][k / 2] and the transposed codes [K][M/2] seen as
-// [k % 8][k / 8][m / 2]: boxes of 128 bytes x rows / 8 (cols / 8) x 8 with
-// the 128-byte swizzle for the persistent kernel, 64 bytes x 16 x 8 with the
-// 64-byte swizzle for the tile kernel.
+// NVFP4: one CTA per tile of NV_TILE_ROWS x NV_TILE_COLS.
+constexpr int NV_TILE_ROWS = 128;
+constexpr int NV_TILE_COLS = 128;
+
+// TMA descriptors of one NVFP4 call: the bf16 input (box one tile), the
+// rowwise codes [M][K/2] seen as [m % 8][m / 8][k / 2] and the transposed
+// codes [K][M/2] seen as [k % 8][k / 8][m / 2] (boxes of 64 bytes x 16 x 8,
+// 64-byte swizzle).
 struct NvMaps {
   CUtensorMap x;
   CUtensorMap q_row;
   CUtensorMap q_t;
 };
 
-// How the NVFP4 kernel for 1D or 2D blocks divides the matrix: one CTA per
-// rows x cols tile (tiles), or a persistent grid walking bands of rows x
-// cols steps.
-struct NvShape {
-  bool tiles;
-  int rows, cols;
-};
-
 struct NvArgs {
   int M, K;
-  int tiles_m, tiles_k;     // row and column counts of nv_shape() tiles / steps
+  int tiles_m, tiles_k;     // tile rows and columns of the grid
   const float* amax;        // device tensor amax
   float* global_scale;      // device, receives amax / 2688
   uint8_t* q_row;
@@ -96,7 +90,7 @@ struct NvArgs {
   uint8_t* s_t;
   uint32_t* dev_err;
   uint64_t timeout_ns;
-  int reverse;              // tile kernel: take the tiles last first
+  int reverse;              // take the tiles last first
 };
 
 // Rows per band (per CTA step) of the MXFP8 kernel for activation `act`.
@@ -109,11 +103,10 @@ cudaError_t launch_mx_tiled(const MxMaps& maps, const MxArgs& a, int mode, bool 
                             int num_sms, cudaStream_t stream);
 cudaError_t launch_dbias_finalize(const float* ws, int bands, int K, float* dbias,
                                   cudaStream_t stream);
-NvShape nv_shape(bool two_d);
 // after_amax: launched right after this call's own bf16_amax grid (as its
 // programmatic dependent).
 cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two_d,
-                         int num_sms, bool after_amax, cudaStream_t stream);
+                         bool after_amax, cudaStream_t stream);
 cudaError_t launch_bf16_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out,
                              int num_sms, cudaStream_t stream);
 cudaError_t launch_nv_global_scale(const float* amax, float* global_scale, cudaStream_t stream);
