@@ -515,11 +515,27 @@ def test_sharded_helpers_single_rank_nccl():
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("M,K", [(96, 256), (1, 8), (333, 72)])
+@pytest.mark.parametrize("M,K", [(96, 256), (1, 8), (333, 72), (4100, 1000), (5, 40000)])
 def test_bf16_amax(M, K):
+    """Blocks of whole rows: one block, several with a partial last one
+    (4100 rows of 2000 bytes), and rows longer than a block's share."""
     bits = synth.nvfp4(M=max(M, 16), K=max(K, 16), seed=48)[:M, :K].copy()
     got = host(mxq.bf16_amax(to_device(bits)))[0]
     assert got == np.float32(oracle.bf16_amax(bits))
+
+
+@pytest.mark.parametrize("where", ["first", "last"])
+def test_bf16_amax_strided_window(where):
+    """ldx > K (a column window of a wider matrix), the largest magnitude in
+    the first or the last row, and larger values outside the window that
+    must not count."""
+    full = synth.nvfp4(M=4100, K=1064, seed=49)
+    full[:, 1000:] = 0x7F00                     # 1.7e38 outside the window
+    r = 0 if where == "first" else 4099
+    full[r, 37] = 0xC700                        # -32768 inside it
+    window = torch.from_numpy(full.view(np.int16)).view(torch.bfloat16).cuda()[:, 8:1000]
+    got = host(mxq.bf16_amax(window))[0]
+    assert got == np.float32(oracle.bf16_amax(full[:, 8:1000].copy())) == np.float32(32768.0)
 
 
 def test_empty_inputs():
