@@ -538,7 +538,7 @@ mxq_status nvfp4_quantize_transpose(const void* x, int64_t M, int64_t K, int64_t
   a.timeout_ns = DEFAULT_TIMEOUT_NS;
   mxq::NvMaps maps{};
   const int mode = direction_mode(flags);
-  st = encode_bf16_map(&maps.x, x, M, K, ldx, mxq::NV_TILE_COLS, mxq::NV_TILE_ROWS);
+  st = encode_bf16_map(&maps.x, x, M, K, ldx, mxq::nv_load_cols(), mxq::NV_TILE_ROWS);
   if (st != MXQ_OK) return st;
   st = encode_nv_code_maps(&maps, flags, M, K, q_row, q_t);
   if (st != MXQ_OK) return st;

@@ -68,8 +68,11 @@ struct MxMaps {
 // NVFP4: one CTA per tile of NV_TILE_ROWS x NV_TILE_COLS.
 constexpr int NV_TILE_ROWS = 128;
 constexpr int NV_TILE_COLS = 128;
+// Columns of one input copy of a tile (the input map's box).
+int nv_load_cols();
 
-// TMA descriptors of one NVFP4 call: the bf16 input (box one tile), the
+// TMA descriptors of one NVFP4 call: the bf16 input (box nv_load_cols()
+// columns x NV_TILE_ROWS rows), the
 // rowwise codes [M][K/2] seen as [m % 8][m / 8][k / 2] and the transposed
 // codes [K][M/2] seen as [k % 8][k / 8][m / 2] (boxes of 64 bytes x 16 x 8,
 // 64-byte swizzle).

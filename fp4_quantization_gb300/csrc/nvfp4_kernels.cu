@@ -11,7 +11,9 @@
 // Layout of the work:
 //  * One CTA (4 warps) per 128 x 128 tile of the input, the grid numbered
 //    along K inside a 128-row band so the block scheduler hands tiles out in
-//    address order; four CTAs share an SM.  One TMA copy brings the tile in.
+//    address order; five CTAs share an SM.  Two TMA copies bring the tile
+//    in, one per 64-column pass; the code staging reuses the first copy's
+//    buffer once pass 0 has read it.
 //  * The tile is taken in two 64-column passes.  Warp w owns rows
 //    32w..32w+31; lane (h, c) = (lane / 8, lane % 8) owns rows 8h..8h+7 and
 //    columns 8c..8c+7 of the pass (eight conflict-free 16-byte shared
@@ -49,17 +51,29 @@ __device__ __forceinline__ uint32_t pick4(const uint32_t v[4], int i) {
   return (i & 2) ? ((i & 1) ? v[3] : v[2]) : ((i & 1) ? v[1] : v[0]);
 }
 
+// Shared memory of a CTA: the tile arrives as two 64-column copies (one per
+// pass), and the code staging reuses the first copy's 16 KiB once pass 0
+// has read it, so a CTA needs 35 KiB; with values widened to fp32 at each
+// use (96 registers) five CTAs share an SM.  Measured on GB300 against one
+// 32 KiB copy, separate staging and four CTAs per SM: 2D 16384 x 8192
+// 65.2 -> 62.6 us, 2D 8192^2 37.0 -> 35.1 us, 1D 16384 x 8192 68.0 -> 68.2
+// (six CTAs per SM spill: 1D 80.2 us).
+constexpr int NT_CPS = 5;                                        // resident CTAs per SM
 constexpr int NT_WARPS = 4;
 constexpr int NT_ROWS = NV_TILE_ROWS;
 constexpr int NT_COLS = NV_TILE_COLS;
 constexpr int NT_TILE_BYTES = NT_ROWS * NT_COLS * 2;            // 32 KiB of bf16
-constexpr int NT_OFF_QR = NT_TILE_BYTES;                         // [m % 8][m / 8][64 B]
+constexpr int NT_LOADS = 2;                                      // input copies per tile
+constexpr int NT_LOAD_BYTES = NT_TILE_BYTES / NT_LOADS;          // [128 rows][128 B] each
+constexpr int NT_OFF_QR = 0;                                     // [m % 8][m / 8][64 B]
 constexpr int NT_OFF_QT = NT_OFF_QR + NT_ROWS * NT_COLS / 2;     // [k % 8][k / 8][64 B]
-constexpr int NT_OFF_RSC = NT_OFF_QT + NT_COLS * NT_ROWS / 2;    // [128 rows][8 blocks]
+constexpr int NT_OFF_RSC = NT_TILE_BYTES;                        // [128 rows][8 blocks]
 constexpr int NT_OFF_TSC = NT_OFF_RSC + NT_ROWS * 8;             // [8 blocks][128 columns]
 constexpr int NT_OFF_INV = NT_OFF_TSC + NT_COLS * 8;             // [128 codes] fp32 1/d
 constexpr int NT_SMEM = NT_OFF_INV + 128 * 4 + 1024;             // + alignment pad
-static_assert(4 * (NT_SMEM + 1024) <= 228 * 1024, "four CTAs per SM");
+static_assert(NT_CPS * (NT_SMEM + 1024) <= 228 * 1024, "CTAs per SM");
+static_assert(NT_OFF_QT + NT_COLS * NT_ROWS / 2 <= NT_LOAD_BYTES,
+              "the staging fits in the first copy's buffer");
 
 // Byte offset inside a [rows][64 B] staging block whose TMA map uses the
 // 64-byte swizzle: the 16-byte chunk index is xor-ed with (row / 2) % 4.
@@ -126,16 +140,16 @@ __device__ __forceinline__ void nv_scales(const uint32_t* m, const NvFastScale& 
 }
 
 template <int MODE, bool TWO_D>
-__global__ void __launch_bounds__(NT_WARPS * 32, 4)
+__global__ void __launch_bounds__(NT_WARPS * 32, NT_CPS)
 nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
                   const __grid_constant__ CUtensorMap tmap_qrow,
                   const __grid_constant__ CUtensorMap tmap_qt, const NvArgs a) {
   constexpr bool ROW = (MODE & MX_ROW) != 0;
   constexpr bool COL = (MODE & MX_COL) != 0;
-  constexpr int ROW_PITCH = NT_COLS * 2;
+  constexpr int ROW_PITCH = NT_LOAD_BYTES / NT_ROWS;   // bytes per row of one input copy
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar;
+  __shared__ __align__(8) uint64_t full_bar[NT_LOADS];
   uint8_t* smem = align_up_shared<1024>(smem_raw);
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x;
@@ -143,7 +157,7 @@ nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int lane = tid & 31;
   const int h = lane >> 3;   // 8-row group 0..3 of the warp's 32 rows
   const int c = lane & 7;    // 8-column chunk 0..7 of the pass's 64 columns
-  const uint32_t bar = smem_addr(&full_bar);
+  const uint32_t bar0 = smem_addr(&full_bar[0]);
   const unsigned t = a.reverse ? gridDim.x - 1u - blockIdx.x : blockIdx.x;
   const int band = static_cast<int>(t / static_cast<unsigned>(a.tiles_k));
   const int tk = static_cast<int>(t) - band * a.tiles_k;
@@ -151,10 +165,15 @@ nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
   if (tid == 0) {
     if (ROW) prefetch_tensormap(&tmap_qrow);
     if (COL) prefetch_tensormap(&tmap_qt);
-    mbar_init(bar, 1);
+#pragma unroll
+    for (int l = 0; l < NT_LOADS; ++l) mbar_init(bar0 + 8 * l, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(bar, NT_TILE_BYTES);
-    tma_load_2d(sbase, &tmap_x, tk * NT_COLS, band * NT_ROWS, bar);
+#pragma unroll
+    for (int l = 0; l < NT_LOADS; ++l) {
+      mbar_arrive_expect_tx(bar0 + 8 * l, NT_LOAD_BYTES);
+      tma_load_2d(sbase + l * NT_LOAD_BYTES, &tmap_x, tk * NT_COLS + l * (NT_COLS / NT_LOADS),
+                  band * NT_ROWS, bar0 + 8 * l);
+    }
   }
   // The tensor amax, read while the copy is in flight (after the amax grid
   // this one may depend on has completed), and the table of 1/d by code
@@ -179,20 +198,23 @@ nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
     sts32(fs.inv_tab + 4 * tid, __float_as_uint(inv));
   }
   __syncthreads();
-  const bool ok = mbar_wait_bounded(bar, 0, a.timeout_ns);
-  if (__syncthreads_or(!ok)) {
-    // The copy never landed: record it, let it finish (bounded) and stop.
-    if (tid == 0) {
-      if (a.dev_err) atomicOr(a.dev_err, 1u);
-      mbar_wait_bounded(bar, 0, a.timeout_ns);
-    }
-    return;
-  }
 
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
+    {
+      const bool ok = mbar_wait_bounded(bar0 + 8 * pass, 0, a.timeout_ns);
+      if (__syncthreads_or(!ok)) {
+        // A copy never landed: record it, let the copies finish (bounded)
+        // and stop.
+        if (tid == 0) {
+          if (a.dev_err) atomicOr(a.dev_err, 1u);
+          for (int l = pass; l < NT_LOADS; ++l) mbar_wait_bounded(bar0 + 8 * l, 0, a.timeout_ns);
+        }
+        return;
+      }
+    }
     // ---- this lane's 8 x 8 block; magnitude maxima ---------------------------
-    const uint32_t my_row0 = sbase + (32 * warp + 8 * h) * ROW_PITCH + (64 * pass + 8 * c) * 2;
+    const uint32_t my_row0 = sbase + pass * NT_LOAD_BYTES + (32 * warp + 8 * h) * ROW_PITCH + 16 * c;
     uint32_t xr[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -226,11 +248,10 @@ nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
       nv_scales<1>(&mm, fs, &code2d, &inv2d);
     }
 
-    float2 xv[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int p = 0; p < 4; ++p) xv[i][p] = make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p]));
+    auto xv = [&](int i, int p) { return make_float2(bf16_lo(xr[i][p]), bf16_hi(xr[i][p])); };
+    // Codes of the pass, stored to the staging below (pass 0 stores them only
+    // after every warp has read the first copy, whose buffer they reuse).
+    uint32_t qrw[8], qtw[8];
 
     // ---- rowwise: block scales (split over the c pair), codes, scale bytes --
     if constexpr (ROW) {
@@ -268,12 +289,11 @@ nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float2 iv = make_float2(rinv[i], rinv[i]);
-        const float2 v0 = mul_f32x2(xv[i][0], iv);
-        const float2 v1 = mul_f32x2(xv[i][1], iv);
-        const float2 v2 = mul_f32x2(xv[i][2], iv);
-        const float2 v3 = mul_f32x2(xv[i][3], iv);
-        sts32(sbase + NT_OFF_QR + swz64(16 * i + 4 * warp + h, 32 * pass + 4 * c),
-              cvt_e2m1x8(v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y));
+        const float2 v0 = mul_f32x2(xv(i, 0), iv);
+        const float2 v1 = mul_f32x2(xv(i, 1), iv);
+        const float2 v2 = mul_f32x2(xv(i, 2), iv);
+        const float2 v3 = mul_f32x2(xv(i, 3), iv);
+        qrw[i] = cvt_e2m1x8(v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y);
       }
       // Scale bytes: the four lanes c = mine, mine + 2, mine + 4, mine + 6
       // hold blocks 0..3 of the pass for the same four rows; lane b = c / 2
@@ -326,16 +346,30 @@ nvfp4_tile_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const float2 iv = make_float2(tinv[2 * p], tinv[2 * p + 1]);
         float2 r[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[i] = mul_f32x2(xv[i][p], iv);
-        const int srow = 16 * (2 * p) + 8 * pass + c;
-        sts32(sbase + NT_OFF_QT + swz64(srow, 16 * warp + 4 * h),
-              cvt_e2m1x8(r[0].x, r[1].x, r[2].x, r[3].x, r[4].x, r[5].x, r[6].x, r[7].x));
-        sts32(sbase + NT_OFF_QT + swz64(srow + 16, 16 * warp + 4 * h),
-              cvt_e2m1x8(r[0].y, r[1].y, r[2].y, r[3].y, r[4].y, r[5].y, r[6].y, r[7].y));
+        for (int i = 0; i < 8; ++i) r[i] = mul_f32x2(xv(i, p), iv);
+        qtw[2 * p] = cvt_e2m1x8(r[0].x, r[1].x, r[2].x, r[3].x, r[4].x, r[5].x, r[6].x, r[7].x);
+        qtw[2 * p + 1] = cvt_e2m1x8(r[0].y, r[1].y, r[2].y, r[3].y, r[4].y, r[5].y, r[6].y, r[7].y);
       }
       // Scale bytes [block][column]: the lane's four columns are adjacent.
       sts32(sbase + NT_OFF_TSC + (2 * warp + (h >> 1)) * NT_COLS + 64 * pass + 8 * c + 4 * mine,
             tcode[0] | (tcode[1] << 8) | (tcode[2] << 16) | (tcode[3] << 24));
+    }
+
+    // ---- the pass's codes to the staging ------------------------------------
+    if (pass == 0) __syncthreads();   // the first copy is read: its buffer is free
+    if constexpr (ROW) {
+      // row i: 4 bytes at byte 32 * pass + 4c of the row's 64; staging row
+      // (m % 8) * 16 + m / 8.
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        sts32(sbase + NT_OFF_QR + swz64(16 * i + 4 * warp + h, 32 * pass + 4 * c), qrw[i]);
+    }
+    if constexpr (COL) {
+      // column k = 64 * pass + 8c + j: 4 bytes at byte 16w + 4h of the
+      // column's 64; staging row (k % 8) * 16 + k / 8.
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        sts32(sbase + NT_OFF_QT + swz64(16 * j + 8 * pass + c, 16 * warp + 4 * h), qtw[j]);
     }
   }
 
@@ -484,6 +518,8 @@ cudaError_t launch_nv_mode(const NvMaps& maps, const NvArgs& a, int mode, bool a
 }
 
 }  // namespace
+
+int nv_load_cols() { return NT_COLS / NT_LOADS; }
 
 cudaError_t launch_nvfp4(const NvMaps& maps, const NvArgs& a, int mode, bool two_d,
                          bool after_amax, cudaStream_t stream) {
