@@ -959,10 +959,14 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
 // CTAs that the block scheduler hands out in address order, which keeps all
 // SMs inside one narrow window of memory.  The plain cast therefore runs as
 // one CTA of 4 warps per 128-row x 128-column tile, tiles numbered along K
-// inside a band: the tile arrives by one TMA copy, the 4 warps take its rows
-// in two 64-row passes (the lane layout and the arithmetic of
-// mx_quantize_kernel), and four CTAs share an SM (at most 128 registers a
-// thread), so one CTA's copy overlaps the others' work.  Rowwise codes leave
+// inside a band: the tile arrives by two TMA copies of 64 rows, the 4 warps
+// take its rows in two 64-row passes (the lane layout and the arithmetic of
+// mx_quantize_kernel), and five CTAs share an SM (at most 96 registers a
+// thread; four with dbias), so one CTA's copies overlap the others' work.
+// The colwise staging reuses the first copy's buffer (36 instead of 53 KiB
+// a CTA; against one copy, separate staging and four CTAs per SM, measured
+// on GB300: 16384^2 162.7 -> 161.7 us, colwise only 122.8 -> 119.4 us).
+// Rowwise codes leave
 // by streaming stores from registers, colwise codes by one bulk tensor store
 // of the staged tile, scale bytes as one 4-byte run per row and column (or
 // one 512-byte tile each in the tiled layout).  With dbias each lane adds
@@ -994,12 +998,23 @@ __device__ __forceinline__ uint64_t tile_policy(int which) {
          : which == 2 ? l2_policy_evict_last() : l2_policy_evict_normal();
 }
 
+// MXQ_TILE_HALVES 1: the tile arrives as two 64-row copies, one per pass,
+// and the colwise staging reuses the first copy's 16 KiB (pass 0 writes it
+// only after the CTA barrier that follows its loads), so a CTA needs 36 KiB
+// and five plain-cast CTAs share an SM (four with dbias); 0: one 32 KiB copy
+// and separate staging, four CTAs per SM.
+#ifndef MXQ_TILE_HALVES
+#define MXQ_TILE_HALVES 1
+#endif
 struct MxTileLayout {
   static constexpr int WARPS = 4;
   static constexpr int ROWS = 128;                           // rows of a tile
+  static constexpr int LOADS = MXQ_TILE_HALVES ? 2 : 1;      // input copies per tile
+  static constexpr int LOAD_ROWS = ROWS / LOADS;
   static constexpr int OFF_TILE = 0;                         // [128 rows][256 B] bf16
-  static constexpr int OFF_QCOL = ROWS * MX_TILE_K * 2;      // [k % 8][k / 8][128 m], 16 KiB
-  static constexpr int OFF_RSC = OFF_QCOL + ROWS * MX_TILE_K;   // [128 rows][4 blocks]
+  static constexpr int OFF_QCOL = MXQ_TILE_HALVES ? 0 : ROWS * MX_TILE_K * 2;   // [k % 8][k / 8][128 m]
+  static constexpr int OFF_RSC = MXQ_TILE_HALVES ? ROWS * MX_TILE_K * 2
+                                                 : OFF_QCOL + ROWS * MX_TILE_K;   // [128 rows][4 blocks]
   static constexpr int OFF_CSC = OFF_RSC + ROWS * 4;            // [128 columns][4 blocks]
   static constexpr int OFF_XCH = OFF_CSC + MX_TILE_K * 4;       // [2 passes][4 warps][16][16 B]
   static constexpr int BYTES = OFF_XCH + 2 * WARPS * 16 * 16;
@@ -1007,7 +1022,7 @@ struct MxTileLayout {
 };
 
 template <int MODE, bool DBIAS>
-__global__ void __launch_bounds__(MxTileLayout::WARPS * 32, 4)
+__global__ void __launch_bounds__(MxTileLayout::WARPS * 32, (MXQ_TILE_HALVES && !DBIAS) ? 5 : 4)
 MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
                const __grid_constant__ CUtensorMap tmap_qcol, const MxArgs a) {
   using L = MxTileLayout;
@@ -1017,7 +1032,7 @@ MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
   constexpr int ROW_PITCH = MX_TILE_K * 2;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar;
+  __shared__ __align__(8) uint64_t full_bar[L::LOADS];
 
   uint8_t* smem = align_up_shared<1024>(smem_raw);
   const uint32_t sbase = smem_addr(smem);
@@ -1026,7 +1041,7 @@ MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
   const int lane = tid & 31;
   const int h = lane >> 4;
   const int c = lane & 15;
-  const uint32_t bar = smem_addr(&full_bar);
+  const uint32_t bar = smem_addr(&full_bar[0]);
   const int band = static_cast<int>(blockIdx.x) / a.tiles_k;
   const int tk = static_cast<int>(blockIdx.x) - band * a.tiles_k;
   // The dbias finalize grid, launched as this grid's programmatic
@@ -1035,18 +1050,18 @@ MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
   if constexpr (DBIAS) grid_launch_dependents();
 
   if (tid == 0) {
-    mbar_init(bar, 1);
+#pragma unroll
+    for (int l = 0; l < L::LOADS; ++l) mbar_init(bar + 8 * l, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(bar, L::ROWS * ROW_PITCH);
-#if MXQ_LOAD_POLICY == 1
-    tma_load_2d_hint(sbase + L::OFF_TILE, &tmap_x, tk * MX_TILE_K, band * L::ROWS, bar,
-                     l2_policy_evict_first());
-#else
-    tma_load_2d(sbase + L::OFF_TILE, &tmap_x, tk * MX_TILE_K, band * L::ROWS, bar);
-#endif
+#pragma unroll
+    for (int l = 0; l < L::LOADS; ++l) {
+      mbar_arrive_expect_tx(bar + 8 * l, L::LOAD_ROWS * ROW_PITCH);
+      tma_load_2d(sbase + L::OFF_TILE + l * L::LOAD_ROWS * ROW_PITCH, &tmap_x, tk * MX_TILE_K,
+                  band * L::ROWS + l * L::LOAD_ROWS, bar + 8 * l);
+    }
   }
   __syncthreads();
-  const bool ok = mbar_wait_bounded(bar, 0, a.timeout_ns);
+  bool ok = mbar_wait_bounded(bar, 0, a.timeout_ns);
 
   const uint32_t ceil_bf16 = a.scale_ceil ? 0x001F001Fu : 0u;
   const int col0 = tk * MX_TILE_K + c * 8;      // first column of this lane
@@ -1058,6 +1073,7 @@ MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
 
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
+    if (L::LOADS == 2 && pass == 1) ok = mbar_wait_bounded(bar + 8, 0, a.timeout_ns);
     const int vw = 4 * pass + warp;             // 16-row slice of the tile, 0..7
     const uint32_t my_row0 = sbase + L::OFF_TILE + (16 * vw + 8 * h) * ROW_PITCH + c * 16;
     uint32_t xr[8][4];
@@ -1096,12 +1112,15 @@ MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
     for (int p = 0; p < 4; ++p) ce[p] = vmax_u16x2(ce[p], __shfl_xor_sync(0xFFFFFFFFu, ce[p], 16));
     const uint32_t xch = sbase + L::OFF_XCH + ((pass * L::WARPS + warp) * 16 + c) * 16;
     if (COL && h == 0) sts128(xch, ce[0], ce[1], ce[2], ce[3]);
-    if (pass == 0) {
+    if (pass < L::LOADS) {
+      // After this barrier every warp has read the pass's copy (with two
+      // copies, pass 0's buffer becomes the colwise staging).
       if (__syncthreads_or(!ok)) {
-        // The copy never landed: record it, let it finish (bounded) and stop.
+        // A copy never landed: record it, let the copies finish (bounded)
+        // and stop.
         if (tid == 0) {
           if (a.dev_err) atomicOr(a.dev_err, 1u);
-          mbar_wait_bounded(bar, 0, a.timeout_ns);
+          for (int l = pass; l < L::LOADS; ++l) mbar_wait_bounded(bar + 8 * l, 0, a.timeout_ns);
         }
         return;
       }
@@ -1471,7 +1490,8 @@ struct MxConfig<ACT_DGEGLU> : MxConfigDGated {};
 template <int MODE, bool DBIAS>
 cudaError_t launch_tile_variant(const MxMaps& maps, const MxArgs& a, cudaStream_t stream) {
   using L = MxTileLayout;
-  static_assert(4 * (L::DYNAMIC + 1024) <= 228 * 1024, "four CTAs per SM must fit");
+  static_assert(((MXQ_TILE_HALVES && !DBIAS) ? 5 : 4) * (L::DYNAMIC + 1024) <= 228 * 1024,
+                "the CTAs per SM must fit");
   static_assert(L::WARPS * 32 == MX_TILE_K && 2 * L::WARPS * 16 * 16 >= 4 * L::WARPS * MX_TILE_K,
                 "dbias: one thread per column; the exchange buffer holds the warps' sums");
   auto kernel = MX_TILE_KERNEL<MODE, DBIAS>;
@@ -1559,6 +1579,13 @@ cudaError_t launch_mode(const MxMaps& maps, const MxArgs& a, int mode, int num_s
 #define MXQ_LAUNCH_NAME launch_mx_tiled
 #else
 #define MXQ_LAUNCH_NAME launch_mx
+int mx_load_rows(int act, bool dbias) {
+  (void)dbias;
+  return (act == ACT_NONE && !MXQ_PLAIN_PERSISTENT && (!dbias || MXQ_DBIAS_TILES))
+             ? MxTileLayout::LOAD_ROWS
+             : mx_band_rows(act);
+}
+
 int mx_band_rows(int act) {
   switch (act) {
     case ACT_GELU: return 16 * MxConfig<ACT_GELU>::WARPS;

@@ -215,7 +215,7 @@ mxq_status rowcol_panel(const void* x, int64_t M, int64_t K, int64_t ldx, uint32
     a.dbias_ws = static_cast<float*>(workspace);
   }
   mxq::MxMaps maps{};
-  st = encode_bf16_map(&maps.x, x, M, K, ldx, mxq::MX_TILE_K, band);
+  st = encode_bf16_map(&maps.x, x, M, K, ldx, mxq::MX_TILE_K, mxq::mx_load_rows(act, want_dbias));
   if (st != MXQ_OK) return st;
   maps.x2 = maps.x;
   if (flags & MXQ_COLWISE) {

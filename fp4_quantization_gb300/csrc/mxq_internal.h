@@ -98,6 +98,9 @@ struct NvArgs {
 
 // Rows per band (per CTA step) of the MXFP8 kernel for activation `act`.
 int mx_band_rows(int act);
+// Rows of one input copy (the input map's box) of the kernel that runs
+// element function `act` (with dbias or not): a band, or half a tile.
+int mx_load_rows(int act, bool dbias);
 
 cudaError_t launch_mx(const MxMaps& maps, const MxArgs& a, int mode, bool dbias, int act,
                       int num_sms, cudaStream_t stream);
