@@ -962,10 +962,11 @@ MX_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
 // inside a band: the tile arrives by two TMA copies of 64 rows, the 4 warps
 // take its rows in two 64-row passes (the lane layout and the arithmetic of
 // mx_quantize_kernel), and five CTAs share an SM (at most 96 registers a
-// thread; four with dbias), so one CTA's copies overlap the others' work.
-// The colwise staging reuses the first copy's buffer (36 instead of 53 KiB
-// a CTA; against one copy, separate staging and four CTAs per SM, measured
-// on GB300: 16384^2 162.7 -> 161.7 us, colwise only 122.8 -> 119.4 us).
+// thread), so one CTA's copies overlap the others' work.  The colwise
+// staging reuses the first copy's buffer (36 instead of 53 KiB a CTA;
+// against one copy, separate staging and four CTAs per SM, measured on
+// GB300: 16384^2 162.7 -> 161.7 us, colwise only 122.8 -> 119.4 us; dbias
+// 8192^2 at five CTAs per SM instead of four 51.5 -> 50.2 us).
 // Rowwise codes leave
 // by streaming stores from registers, colwise codes by one bulk tensor store
 // of the staged tile, scale bytes as one 4-byte run per row and column (or
@@ -1001,10 +1002,13 @@ __device__ __forceinline__ uint64_t tile_policy(int which) {
 // MXQ_TILE_HALVES 1: the tile arrives as two 64-row copies, one per pass,
 // and the colwise staging reuses the first copy's 16 KiB (pass 0 writes it
 // only after the CTA barrier that follows its loads), so a CTA needs 36 KiB
-// and five plain-cast CTAs share an SM (four with dbias); 0: one 32 KiB copy
-// and separate staging, four CTAs per SM.
+// and MXQ_TILE_CPS CTAs share an SM; 0: one 32 KiB copy and separate
+// staging, four CTAs per SM (tuning comparisons).
 #ifndef MXQ_TILE_HALVES
 #define MXQ_TILE_HALVES 1
+#endif
+#ifndef MXQ_TILE_CPS
+#define MXQ_TILE_CPS 5
 #endif
 struct MxTileLayout {
   static constexpr int WARPS = 4;
@@ -1022,7 +1026,7 @@ struct MxTileLayout {
 };
 
 template <int MODE, bool DBIAS>
-__global__ void __launch_bounds__(MxTileLayout::WARPS * 32, (MXQ_TILE_HALVES && !DBIAS) ? 5 : 4)
+__global__ void __launch_bounds__(MxTileLayout::WARPS * 32, MXQ_TILE_HALVES ? MXQ_TILE_CPS : 4)
 MX_TILE_KERNEL(const __grid_constant__ CUtensorMap tmap_x,
                const __grid_constant__ CUtensorMap tmap_qcol, const MxArgs a) {
   using L = MxTileLayout;
@@ -1490,7 +1494,7 @@ struct MxConfig<ACT_DGEGLU> : MxConfigDGated {};
 template <int MODE, bool DBIAS>
 cudaError_t launch_tile_variant(const MxMaps& maps, const MxArgs& a, cudaStream_t stream) {
   using L = MxTileLayout;
-  static_assert(((MXQ_TILE_HALVES && !DBIAS) ? 5 : 4) * (L::DYNAMIC + 1024) <= 228 * 1024,
+  static_assert((MXQ_TILE_HALVES ? MXQ_TILE_CPS : 4) * (L::DYNAMIC + 1024) <= 228 * 1024,
                 "the CTAs per SM must fit");
   static_assert(L::WARPS * 32 == MX_TILE_K && 2 * L::WARPS * 16 * 16 >= 4 * L::WARPS * MX_TILE_K,
                 "dbias: one thread per column; the exchange buffer holds the warps' sums");
